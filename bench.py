@@ -1,0 +1,442 @@
+"""Benchmark of the GB300 Q2_K MoE-FFN layer (one JSON line on stdout).
+
+Default workload: the Qwen3.6-35B-A3B-shaped decode layer at batch 1 (hidden
+2048, 256 routed experts, top-8, expert ffn 512, bf16 shared expert ffn 512,
+bf16 x), four distinct layer copies cycled, 64-token x pool.  A step is one
+call of the whole layer (router, top-k, grouping, routed gate/up + SwiGLU,
+down + combine, gated shared expert) on the step's tokens.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens T]
+                  [--impl ours|reference] [--no-flush]
+
+Timing: W untimed warm-up steps, then K steps.  Inputs are resident in HBM.
+Between timed steps the L2 is flushed (a 512 MiB write, then a 256 MiB read so
+the cache holds clean lines) outside the step's CUDA-event pair; the step time
+is the sum of the per-step event intervals on the launching stream, max over
+ranks.  `e2e` times the same call through the public API with the step's x
+copied in from pinned host memory and y copied back, inside the events.
+
+Expert weights are drawn N(0, 0.02) on the device with torch's seeded
+generator and quantised by the library's Q2_K encoder; x, router, bias and
+shared-expert weights come from the shared seeded generators (qs_inputs).
+`--impl reference` times the oracle (plain C, double precision) on the host
+cores on the same workload: that is this layer's reference implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qs_inputs as qi  # noqa: E402
+
+L2_FLUSH_WRITE = 512 << 20
+L2_FLUSH_READ = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_35b_a3b", choices=sorted(qi.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-flush", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+class Dist:
+    def __init__(self, n_gpus):
+        import torch
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            torch.cuda.set_device(self.local)
+            dist.init_process_group("nccl")
+            self.pg = dist
+        elif n_gpus > 1:
+            raise SystemExit("--gpus > 1 needs torchrun (one process per GPU)")
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ the oracle on host cores
+
+def oracle_sample_layer(w, T, n_tokens, copy=0):
+    """Host layer for the oracle: x pool tokens 0..n_tokens-1, experts those tokens route to."""
+    import oracle
+    import concurrent.futures as cf
+    sh = w.shape
+    xb, _ = qi.gen_x(sh, w.seed, n_tokens)
+    Wr = qi.gen_router(sh, w.seed, copy)
+    bias = qi.gen_bias(sh, w.seed, copy, w.zipf_bias)
+    shared = qi.gen_shared(sh, w.seed, copy)
+    ids, _, _, _ = oracle.route(xb, oracle.X_BF16 if sh.x_dtype == qi.BF16 else oracle.X_F32, Wr, bias, sh.top_k)
+    blob = np.zeros(sh.n_experts * sh.expert_bytes, np.uint8)
+
+    def one(e):
+        blob[e * sh.expert_bytes:(e + 1) * sh.expert_bytes] = oracle.quantize_expert(
+            *qi.gen_expert_f32(sh, w.seed, copy, int(e)))
+
+    with cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
+        list(ex.map(one, np.unique(ids)))
+    return xb, Wr, bias, shared, blob
+
+
+def time_oracle(w, T, budget_s, max_calls=None):
+    """Run the oracle, one layer call of T tokens at a time on one core, for ~budget_s seconds."""
+    import oracle
+    n_pool = 16 if T == 1 else max(T, 16)
+    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
+    calls, tokens = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        t_start = (calls * T) % max(1, n_pool - T + 1)
+        oracle.moe_ffn(w.shape, xb[t_start:t_start + T], Wr, bias, blob, w.shape.expert_bytes, shared)
+        calls += 1
+        tokens += T
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_calls and calls >= max_calls):
+            break
+    return tokens / el, calls, el
+
+
+def cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def run_reference(args, w, T):
+    """The reference arm: the oracle on host cores, same metric, unit and config."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n_pool = max(T, 16)
+    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
+
+    def step(i):
+        t0 = (i * T) % max(1, n_pool - T + 1)
+        oracle.moe_ffn(w.shape, xb[t0:t0 + T], Wr, bias, blob, w.shape.expert_bytes, shared)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    el = time.perf_counter() - t0
+    ms = el / args.steps * 1e3
+    val = T * args.steps / el
+    line = {
+        "impl": "reference", "metric": "MoE-FFN layer tokens/s (batch %d decode)" % T, "value": val,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, T, args),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} layer calls of {T} token(s) over a {n_pool}-token x pool, "
+                                   f"experts those tokens route to; {cpu_model()}"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, T, args):
+    s = w.shape
+    return {"workload": w.name, "hidden": s.hidden, "n_experts": s.n_experts, "top_k": s.top_k,
+            "expert_ffn": s.expert_ffn, "shared_ffn": s.shared_ffn, "n_tokens": T, "layer_copies": w.copies,
+            "x_pool": qi.X_POOL, "expert_format": "Q2_K (84 B / 256 weights)", "zipf_bias": w.zipf_bias,
+            "l2": "no flush (copies cycled)" if args.no_flush else
+                  "flushed between timed steps (512 MiB write + 256 MiB read, outside the events)",
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def device_layers(w, qm, torch, device):
+    """Layer copies resident in HBM: experts quantised on the device, the rest from qs_inputs."""
+    sh = w.shape
+    H, E, k, F, S = sh.hidden, sh.n_experts, sh.top_k, sh.expert_ffn, sh.shared_ffn
+    stride = sh.expert_bytes
+    gbytes = F * H // 256 * 84
+    layers = []
+    for c in range(w.copies):
+        gen = torch.Generator(device=device)
+        gen.manual_seed(qi.stream_of(w.seed, c))
+        blob = torch.empty(E * stride, dtype=torch.uint8, device=device)
+        chunk = max(1, min(E, (256 << 20) // (4 * F * H)))
+        for e0 in range(0, E, chunk):
+            n = min(chunk, E - e0)
+            for rows, cols, off in ((F, H, 0), (F, H, gbytes), (H, F, 2 * gbytes)):
+                wts = torch.randn((n, rows, cols), generator=gen, device=device, dtype=torch.float32) * 0.02
+                for i in range(n):
+                    base = blob.data_ptr() + (e0 + i) * stride + off
+                    qm.qs_q2k_quantize(wts[i], base)
+        Wr = torch.from_numpy(qi.gen_router(sh, w.seed, c)).to(device)
+        b = qi.gen_bias(sh, w.seed, c, w.zipf_bias)
+        bias = None if b is None else torch.from_numpy(b).to(device)
+        shh = qi.gen_shared(sh, w.seed, c)
+        shd = {n_: torch.from_numpy(v.view(np.int16)).to(device) for n_, v in shh.items()}
+        layers.append({"blob": blob, "experts": qm.make_experts(blob, stride), "Wr": Wr, "bias": bias, "sh": shd,
+                       "shared": qm.make_shared(shd["gate"], shd["up"], shd["down"], shd["sig"])})
+    torch.cuda.synchronize()
+    return layers
+
+
+def algorithmic_bytes(sh, T, distinct):
+    """Bytes the layer must move for one call: router, x, the distinct experts' Q2_K, shared, out."""
+    router = sh.n_experts * sh.hidden * 4
+    x = T * sh.hidden * (2 if sh.x_dtype == qi.BF16 else 4)
+    experts = distinct * sh.expert_bytes
+    shared = (3 * sh.shared_ffn * sh.hidden + sh.hidden) * 2
+    out = T * sh.hidden * 4
+    return router + x + experts + shared + out, experts
+
+
+def run_ours(args, w, T):
+    import torch
+    dist = Dist(args.gpus)
+    device = torch.device("cuda", dist.local)
+    torch.cuda.set_device(device)
+    import __graft_entry__
+    __graft_entry__.build()
+    from bit_quantized_moe_router_gb300 import qs_moe as qm
+    qm.load(build_if_missing=False)
+    sh = w.shape
+    H = sh.hidden
+    shape = qm.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.expert_ffn, sh.shared_ffn, sh.x_dtype)
+    layers = device_layers(w, qm, torch, device)
+    launches_per_step = qm.qs_moe_ffn_launches(shape, T, True)
+    if launches_per_step < 1:
+        raise SystemExit(f"qs_moe_ffn_launches failed ({launches_per_step})")
+
+    # x pool: rows wrap so that rows [j, j+T) are contiguous for every j < X_POOL
+    xb, _ = qi.gen_x(sh, w.seed, qi.X_POOL)
+    xwrap = np.concatenate([xb, xb[:T]], axis=0)
+    xdev = torch.from_numpy(xwrap.view(np.int16) if xwrap.dtype == np.uint16 else xwrap).to(device)
+    ws = qm.alloc_workspace(shape, T)
+    out = torch.empty((T, H), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def xs(i):
+        j = (i * T) % qi.X_POOL
+        return xdev[j:j + T]
+
+    def step(i, x=None):
+        Ld = layers[i % len(layers)]
+        qm.qs_moe_ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T,
+                      ws, stream)
+
+    # distinct experts per step (routing is a function of the copy and the x rows)
+    ids = torch.empty((T, sh.top_k), dtype=torch.int32, device=device)
+    pw = torch.empty((T, sh.top_k), dtype=torch.float32, device=device)
+    import math
+    period = math.lcm(len(layers), qi.X_POOL // math.gcd(T, qi.X_POOL))
+    distinct = []
+    for i in range(period):
+        Ld = layers[i % len(layers)]
+        qm.qs_route_topk(shape, xs(i), Ld["Wr"], Ld["bias"], T, ids, pw, ws, stream)
+        distinct.append(len(torch.unique(ids).tolist()))
+    qm.qs_workspace_init(ws, stream)
+
+    flush_w = torch.empty(L2_FLUSH_WRITE, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(L2_FLUSH_READ // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        if not args.no_flush:
+            flush_w.zero_()
+            flush_r.sum()
+
+    for i in range(args.warmup):
+        flush()
+        step(i)
+    torch.cuda.synchronize()
+    st = qm.qs_read_device_status(ws, stream)
+    if st != qm.QS_OK:
+        raise SystemExit(f"device status after warm-up: {qm.status_string(st)}")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dist.local if dist.world > 1 else torch.cuda.current_device())
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush()
+        evs[i][0].record(stream)
+        step(args.warmup + i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    dist.barrier()
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in evs])
+    total_s = dist.max(float(step_ms.sum()) / 1e3)
+    st = qm.qs_read_device_status(ws, stream)
+    if st != qm.QS_OK:
+        raise SystemExit(f"device status after the timed steps: {qm.status_string(st)}")
+
+    # e2e through the public API: pinned host x in, y back out, inside the events
+    x_host = torch.from_numpy(xwrap.view(np.int16) if xwrap.dtype == np.uint16 else xwrap).pin_memory()
+    y_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    x_stage = torch.empty_like(xdev[:T])
+    e2e_ms = []
+    for i in range(K):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        j = ((args.warmup + i) * T) % qi.X_POOL
+        x_stage.copy_(x_host[j:j + T], non_blocking=True)
+        step(args.warmup + i, x=x_stage)
+        y_host.copy_(out, non_blocking=True)
+        b.record(stream)
+        e2e_ms.append((a, b))
+    torch.cuda.synchronize()
+    e2e_s = dist.max(sum(a.elapsed_time(b) for a, b in e2e_ms) / 1e3)
+
+    # roofline of the layer kernel(s): algorithmic bytes over the measured step time
+    steps_idx = [(args.warmup + i) % len(distinct) for i in range(K)]
+    algo = [algorithmic_bytes(sh, T, distinct[j]) for j in steps_idx]
+    algo_bytes = float(np.mean([a for a, _ in algo]))
+    q2k_bytes = float(np.mean([q for _, q in algo]))
+    mean_step_s = total_s / K
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    achieved = algo_bytes / mean_step_s / 1e9
+    tokens_total = T * K * dist.world
+    value = tokens_total / total_s
+    if dist.rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and dist.world == 1:
+        rate, calls, el = time_oracle(w, T, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{calls} layer calls of {T} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
+                         f"the experts they route to; {cpu_model()}"}
+    line = {
+        "metric": "MoE-FFN layer tokens/s (batch %d decode)" % T,
+        "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": mean_step_s * 1e3, "us_per_layer": mean_step_s * 1e6,
+        "us_per_layer_p10_p50_p90": [float(np.percentile(step_ms, q) * 1e3) for q in (10, 50, 90)],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "q2k-int16dot-f32", "data": "synthetic",
+        "config": config_of(w, T, args),
+        "achieved_gbs_all_bytes": achieved, "achieved_gbs_q2k_bytes": q2k_bytes / mean_step_s / 1e9,
+        "roofline": {"bound": "hbm",
+                     "kernel": "fused_decode_kernel" if launches_per_step == 1 else "qs_moe_ffn (whole layer)", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
+                     "algorithmic_bytes_per_launch": algo_bytes, "traffic": None},
+        "e2e": {"value": tokens_total / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_stage.numel() * x_stage.element_size()),
+                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+        "gpu_launches": None,
+        "clocks": clk,
+        "bracket_wall_s": wall,
+        "cpu_baseline": cpu,
+    }
+    line["gpu_launches"] = launches_per_step * K
+    line["kernels_per_step"] = launches_per_step
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    w = qi.WORKLOADS[args.workload]
+    T = args.tokens or w.tokens[0]
+    if args.impl == "reference":
+        run_reference(args, w, T)
+    else:
+        run_ours(args, w, T)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,693 @@
+// qs_decode.cu -- the per-step kernels of the Q2_K MoE-FFN layer (sm_103a).
+//
+//   route_kernel          (a) router GEMV (fp32) + softmax + warp-shuffle top-k
+//   group_kernel          (b) token -> expert grouping (stable counting sort)
+//   gateup_kernel         (c) grouped Q2_K gate+up dequant-GEMV, SwiGLU epilogue
+//   down_kernel           (d) Q2_K down GEMV + routing-weight combine (+ shared down)
+//   shared_gateup_kernel      bf16 shared-expert gate/up GEMV + sigmoid gate
+//   quantize_kernel           Q2_K encoder (weight set-up)
+//
+// Q2_K dot products.  A 256-weight block is split into four 64-weight chunks
+// u = 0..3: chunk u is qs bytes 16u..16u+15, i.e. weights 128h + 32j + 16(u&1)
+// + c for h = u>>1, shift j = 0..3, c = 0..15 -- four sub-blocks of 16.  One
+// thread owns one chunk of one block for every row it visits, so the matching
+// activations stay in registers.  Activations are quantised per token to int16
+// with a max-abs scale; a sub-block dot is then sum_c q_c * x_c, taken exactly
+// in int32 with dp2a (16-bit x 8-bit) on the masked code bytes.  Masking bits
+// 2j..2j+1 without shifting gives bytes q * 4^j, divided out exactly by an
+// arithmetic shift of the sum.  Scale and min nibbles then weight the exact
+// integer sums, and one fp32 FMA pair per chunk applies fp16 d and dmin:
+//   sum_i w_i x_i = s_x * (d * sum_sb sc_lo[sb] * S_sb - dmin * sum_sb sc_hi[sb] * X_sb)
+// with S_sb = sum q*xq and X_sb = sum xq over sub-block sb.
+#include "qs_common.cuh"
+#include "qs_internal.h"
+#include "qs_q2k.cuh"
+
+#include <algorithm>
+
+namespace qs {
+
+// ====================================================================== (a) router
+
+constexpr int kRouteWarps = 2;  // expert rows per router CTA (one warp each)
+
+// grid (ceil(E / kRouteWarps), ceil(T / kRouteTok)), block 32 * kRouteWarps.
+// dynamic smem: kRouteTok * H floats (the token chunk, widened to fp32).
+__global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(const void* __restrict__ x, int x_dtype,
+                                                                  const float* __restrict__ W,
+                                                                  const float* __restrict__ bias, int H, int E,
+                                                                  int k, int T, float* logits, int32_t* ids,
+                                                                  float* pw, uint32_t* tickets) {
+    extern __shared__ __align__(16) float xs[];
+    __shared__ uint32_t s_last;
+    const int chunk = blockIdx.y;
+    const int t0 = chunk * kRouteTok;
+    const int nt = min(kRouteTok, T - t0);
+    for (int i = threadIdx.x; i < nt * H; i += blockDim.x) xs[i] = load_x(x, x_dtype, (size_t)t0 * H + i);
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kRouteWarps + warp;
+    if (e < E) {
+        float acc[kRouteTok];
+#pragma unroll
+        for (int t = 0; t < kRouteTok; t++) acc[t] = 0.0f;
+        const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)e * H);
+        for (int i = lane; i < H / 4; i += 32) {
+            const float4 w = __ldg(w4 + i);
+#pragma unroll
+            for (int t = 0; t < kRouteTok; t++) {
+                if (t < nt) {
+                    const float4 xv = reinterpret_cast<const float4*>(xs + t * H)[i];
+                    acc[t] = fmaf(w.x, xv.x, acc[t]);
+                    acc[t] = fmaf(w.y, xv.y, acc[t]);
+                    acc[t] = fmaf(w.z, xv.z, acc[t]);
+                    acc[t] = fmaf(w.w, xv.w, acc[t]);
+                }
+            }
+        }
+        const float b = bias ? bias[e] : 0.0f;
+#pragma unroll
+        for (int t = 0; t < kRouteTok; t++) {
+            const float s = warp_sum(acc[t]);
+            if (lane == 0 && t < nt) logits[(size_t)(t0 + t) * E + e] = s + b;
+        }
+    }
+    // last CTA of this token chunk does the top-k (no grid-wide wait)
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&tickets[chunk], 1u) == gridDim.x - 1) ? 1u : 0u;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int t = warp; t < nt; t += kRouteWarps)
+        topk_softmax_warp(logits + (size_t)(t0 + t) * E, E, k, ids + (size_t)(t0 + t) * k, pw + (size_t)(t0 + t) * k);
+    if (threadIdx.x == 0) tickets[chunk] = 0u;  // ready for the next call
+}
+
+// ====================================================================== (b) grouping
+
+// One CTA of 32*NW threads.  smem: hist[NW][E] + off[E+1] ints.
+__global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int n, int E,
+                                                     int32_t* counts, int32_t* offsets, int32_t* perm) {
+    extern __shared__ int32_t gsm[];
+    const int NW = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* hist = gsm;
+    int32_t* off = gsm + NW * E;
+    for (int i = threadIdx.x; i < NW * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const int seg = (n + NW - 1) / NW;
+    const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
+    for (int i = s0 + lane; i < s1; i += 32) {
+        const int e = ids[i];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&hist[warp * E + e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < NW; w++) {
+            const int c = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += c;
+        }
+        off[e] = run;  // count, scanned below
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = (e < E) ? off[e] : 0;
+            int s = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            if (e < E) {
+                counts[e] = c;
+                off[e] = carry + s - c;
+                offsets[e] = carry + s - c;
+            }
+            carry += __shfl_sync(0xffffffffu, s, 31);
+        }
+        if (lane == 0) {
+            off[E] = carry;
+            offsets[E] = carry;
+        }
+    }
+    __syncthreads();
+    for (int base = s0; base < s1; base += 32) {
+        const int i = base + lane;
+        const int e = (i < s1) ? ids[i] : -1;
+        const bool valid = (i < s1) && (unsigned)e < (unsigned)E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+        if (valid) {
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            perm[off[e] + hist[warp * E + e] + rank] = i;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+        __syncwarp();
+    }
+}
+
+// Quantise n fp32 values (read by f(i)) to int16 in shared memory; returns the scale.
+template <class Load>
+__device__ __forceinline__ float quantize_to_smem(Load f, int n, int16_t* xq, float* red) {
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) m = fmaxf(m, fabsf(f(i)));
+    m = block_max(m, red);
+    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) xq[i] = (int16_t)__float2int_rn(f(i) * inv);
+    __syncthreads();
+    return m * (1.0f / 32767.0f);
+}
+
+// Sum partials of the tpr threads that share a row.  Power-of-two tpr <= 32:
+// butterfly inside the aligned lane group; otherwise through shared memory in
+// a fixed order.  Every thread of the block must call it (contains barriers
+// on the shared-memory path).  Result valid in the row's first thread.
+__device__ __forceinline__ float row_reduce(float v, int tpr, float* scratch) {
+    if ((tpr & (tpr - 1)) == 0 && tpr <= 32) {
+        for (int o = tpr >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        return v;
+    }
+    __syncthreads();
+    scratch[threadIdx.x] = v;
+    __syncthreads();
+    float s = 0.0f;
+    if (threadIdx.x % tpr == 0 && threadIdx.x + tpr <= blockDim.x)
+        for (int i = 0; i < tpr; i++) s += scratch[threadIdx.x + i];
+    return s;
+}
+
+// Bounded wait on an mbarrier phase with a block-uniform outcome: thread 0
+// waits (bounded), the result is broadcast, then every thread acquires the
+// completed phase (which returns at once) so the copied bytes are visible.
+__device__ __forceinline__ bool block_mbar_wait(uint64_t* bar, uint32_t parity, int32_t* flag) {
+    if (threadIdx.x == 0) *flag = mbar_wait(bar, parity) ? 1 : 0;
+    __syncthreads();
+    const bool ok = *flag != 0;
+    if (ok)
+        while (!mbar_try_wait(bar, parity)) {
+        }
+    return ok;
+}
+
+// ====================================================================== (c) gate/up
+
+constexpr int kGemvThreads = 256;
+
+struct alignas(16) GateUpSmem {
+    uint64_t bar;
+    float red[32];
+    int32_t expert;
+    int32_t ok;
+};
+
+// grid.x = max_active * (F / R); block kGemvThreads.
+// dynamic smem: GateUpSmem | xq int16[H] (padded to 16) | scratch f32[256] | weights 2 * R * rowbytes.
+__global__ void __launch_bounds__(kGemvThreads) gateup_kernel(const void* __restrict__ x, int x_dtype, int H, int E,
+                                                              int k, int F, int R, const uint8_t* __restrict__ experts,
+                                                              int64_t stride, const int32_t* __restrict__ offsets,
+                                                              const int32_t* __restrict__ perm, float* h_out) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    GateUpSmem& S = *reinterpret_cast<GateUpSmem*>(smem);
+    int16_t* xq = reinterpret_cast<int16_t*>(smem + sizeof(GateUpSmem));
+    float* scratch = reinterpret_cast<float*>(smem + sizeof(GateUpSmem) + ((size_t)H * 2 + 15) / 16 * 16);
+    uint8_t* wbuf = reinterpret_cast<uint8_t*>(scratch + kGemvThreads);
+    const int nb = H / kBlockWeights;
+    const int rowbytes = nb * kBlockBytes;
+    const int tiles = F / R;
+    const int a = blockIdx.x / tiles, tile = blockIdx.x % tiles;
+
+    // the a-th active expert (ascending id)
+    if (threadIdx.x == 0) S.expert = -1;
+    __syncthreads();
+    {
+        int base = 0;
+        for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+            const int e = e0 + threadIdx.x;
+            const bool act = e < E && offsets[e + 1] > offsets[e];
+            // block-wide exclusive prefix of act
+            const unsigned bal = __ballot_sync(0xffffffffu, act);
+            const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+            if (lane == 0) S.red[warp] = __int_as_float(__popc(bal));
+            __syncthreads();
+            int before = base;
+            for (int w = 0; w < warp; w++) before += __float_as_int(S.red[w]);
+            before += __popc(bal & ((1u << lane) - 1u));
+            if (act && before == a) S.expert = e;
+            int tot = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); w++) tot += __float_as_int(S.red[w]);
+            base += tot;
+            __syncthreads();
+        }
+    }
+    const int e = S.expert;
+    if (e < 0) return;  // fewer active experts than the grid allows for
+
+    const uint8_t* gate_rows = experts + (int64_t)e * stride + (int64_t)tile * R * rowbytes;
+    const uint8_t* up_rows = gate_rows + (int64_t)F * rowbytes;
+    const uint32_t tile_bytes = (uint32_t)R * rowbytes;
+    if (threadIdx.x == 0) {
+        mbar_init(&S.bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&S.bar, 2 * tile_bytes);
+        bulk_g2s(wbuf, gate_rows, tile_bytes, &S.bar);
+        bulk_g2s(wbuf + tile_bytes, up_rows, tile_bytes, &S.bar);
+    }
+
+    const int tpr = 4 * nb;
+    const int rows_par = kGemvThreads / tpr;
+    const int rg = threadIdx.x / tpr, c = threadIdx.x % tpr;
+    const bool lane_active = rg < rows_par;  // threads past the last whole row group idle
+    const int b = c >> 2, u = c & 3;
+    const int j0 = offsets[e], j1 = offsets[e + 1];
+    bool waited = false;
+    for (int j = j0; j < j1; j++) {
+        const int entry = perm[j];
+        const int t = entry / k;
+        const float sx = quantize_to_smem([&](int i) { return load_x(x, x_dtype, (size_t)t * H + i); }, H, xq, S.red);
+        XFrag f;
+        load_xfrag(xq, b, u, f);
+        if (!waited) {
+            if (!block_mbar_wait(&S.bar, 0, &S.ok)) return;  // copy never completed: outputs left unwritten
+            waited = true;
+        }
+        for (int r0 = 0; r0 < R; r0 += rows_par) {
+            const int r = lane_active ? r0 + rg : R;
+            float g = 0.0f, uu = 0.0f;
+            if (r < R) {
+                g = q2k_chunk_dot(wbuf + (size_t)r * rowbytes + b * kBlockBytes, u, f);
+                uu = q2k_chunk_dot(wbuf + tile_bytes + (size_t)r * rowbytes + b * kBlockBytes, u, f);
+            }
+            g = row_reduce(g, tpr, scratch);
+            uu = row_reduce(uu, tpr, scratch);
+            if (r < R && c == 0) h_out[(size_t)entry * F + tile * R + r] = silu(sx * g) * (sx * uu);
+        }
+        __syncthreads();  // xq is rewritten for the next token
+    }
+    if (!waited) block_mbar_wait(&S.bar, 0, &S.ok);  // never leave a copy in flight into freed shared memory
+}
+
+// ====================================================================== (d) down + combine
+
+constexpr int kDownThreads = 128;
+constexpr int kMaxSlots = 32;
+
+struct alignas(16) DownSmem {
+    uint64_t bar;
+    float red[32];
+    float sh[kMaxSlots];      // scale of each slot's quantised h
+    float p[kMaxSlots];       // routing weight of each slot
+    int32_t eid[kMaxSlots];   // expert of each slot (ascending)
+    int32_t hrow[kMaxSlots];  // row of h for each slot
+    int32_t ok;
+};
+
+// grid (H / R, T); block kDownThreads.
+// dynamic smem: DownSmem | xq int16[G][F] | scratch f32[kDownThreads] | weights G * R * rowbytes.
+__global__ void __launch_bounds__(kDownThreads) down_kernel(int H, int k, int F, int S, int R, int G,
+                                                            const uint8_t* __restrict__ experts, int64_t stride,
+                                                            const float* __restrict__ h, const int32_t* __restrict__ ids,
+                                                            const float* __restrict__ pw, int n_slots,
+                                                            const uint16_t* __restrict__ sh_down,
+                                                            const float* __restrict__ hs,
+                                                            const float* __restrict__ gate, float* out,
+                                                            int accumulate) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    DownSmem& D = *reinterpret_cast<DownSmem*>(smem);
+    int16_t* xq = reinterpret_cast<int16_t*>(smem + sizeof(DownSmem));
+    float* scratch = reinterpret_cast<float*>(smem + sizeof(DownSmem) + ((size_t)G * F * 2 + 15) / 16 * 16);
+    uint8_t* wbuf = reinterpret_cast<uint8_t*>(scratch + kDownThreads);
+    const int t = blockIdx.y;
+    const int r0 = blockIdx.x * R;
+    const int nbF = F / kBlockWeights;
+    const int rowbytes = nbF * kBlockBytes;
+    const int64_t down_off = 2ll * F * (H / kBlockWeights) * kBlockBytes;
+    const uint32_t tile_bytes = (uint32_t)R * rowbytes;
+
+    if (threadIdx.x == 0) {
+        // slots of this token sorted by expert id (fixed summation order)
+        for (int s = 0; s < n_slots; s++) {
+            const int e = ids[(size_t)t * k + s];
+            int pos = s;
+            while (pos > 0 && D.eid[pos - 1] > e) {
+                D.eid[pos] = D.eid[pos - 1];
+                D.p[pos] = D.p[pos - 1];
+                D.hrow[pos] = D.hrow[pos - 1];
+                pos--;
+            }
+            D.eid[pos] = e;
+            D.p[pos] = pw[(size_t)t * k + s];
+            D.hrow[pos] = t * k + s;
+        }
+        mbar_init(&D.bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int tpr = 4 * nbF;
+    const int rows_par = kDownThreads / tpr;
+    const int rg = threadIdx.x / tpr, c = threadIdx.x % tpr;
+    const bool lane_active = rg < rows_par;
+    const int b = c >> 2, u = c & 3;
+    const int rpt = (R + rows_par - 1) / rows_par;  // rows per thread group (<= 4)
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    bool ok = true;
+
+    for (int g0 = 0, phase = 0; g0 < n_slots; g0 += G, phase ^= 1) {
+        const int ng = min(G, n_slots - g0);
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&D.bar, ng * tile_bytes);
+            for (int s = 0; s < ng; s++)
+                bulk_g2s(wbuf + (size_t)s * tile_bytes,
+                         experts + (int64_t)D.eid[g0 + s] * stride + down_off + (int64_t)r0 * rowbytes, tile_bytes,
+                         &D.bar);
+        }
+        for (int s = 0; s < ng; s++) {
+            const float* hr = h + (size_t)D.hrow[g0 + s] * F;
+            const float sc = quantize_to_smem([&](int i) { return __ldcg(hr + i); }, F, xq + (size_t)s * F, D.red);
+            if (threadIdx.x == 0) D.sh[g0 + s] = sc;
+        }
+        if (!block_mbar_wait(&D.bar, phase, &D.ok)) {
+            ok = false;
+            break;
+        }
+        for (int s = 0; s < ng; s++) {
+            XFrag f;
+            load_xfrag(xq + (size_t)s * F, b, u, f);
+            const float ps = D.p[g0 + s] * D.sh[g0 + s];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const int r = lane_active ? rg + i * rows_par : R;
+                if (i < rpt) {
+                    float v = 0.0f;
+                    if (r < R) v = q2k_chunk_dot(wbuf + (size_t)s * tile_bytes + (size_t)r * rowbytes + b * kBlockBytes, u, f);
+                    v = row_reduce(v, tpr, scratch);
+                    if (r < R && c == 0) acc[i] = fmaf(ps, v, acc[i]);
+                }
+            }
+        }
+        __syncthreads();  // buffers are reused by the next group
+    }
+    if (!ok) return;
+
+    // results of the routed part live in the first thread of each row group; move to smem
+    float* res = scratch;  // R floats (R <= kDownThreads)
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int r = lane_active ? rg + i * rows_par : R;
+        if (i < rpt && r < R && c == 0) res[r] = acc[i];
+    }
+    if (n_slots == 0)
+        for (int r = threadIdx.x; r < R; r += blockDim.x) res[r] = 0.0f;
+    __syncthreads();
+
+    // shared expert down rows: one warp per row, bf16 weights x fp32 hs
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (sh_down != nullptr && S > 0) {
+        const float gt = gate[t];
+        const float* hst = hs + (size_t)t * S;
+        for (int r = warp; r < R; r += kDownThreads / 32) {
+            const uint4* wr = reinterpret_cast<const uint4*>(sh_down + (size_t)(r0 + r) * S);
+            float a2 = 0.0f;
+            for (int i = lane; i < S / 8; i += 32) {
+                const uint4 w = __ldg(wr + i);
+                const float4 h0 = __ldcg(reinterpret_cast<const float4*>(hst) + 2 * i);
+                const float4 h1 = __ldcg(reinterpret_cast<const float4*>(hst) + 2 * i + 1);
+                a2 = fmaf(bf16_lo(w.x), h0.x, a2);
+                a2 = fmaf(bf16_hi(w.x), h0.y, a2);
+                a2 = fmaf(bf16_lo(w.y), h0.z, a2);
+                a2 = fmaf(bf16_hi(w.y), h0.w, a2);
+                a2 = fmaf(bf16_lo(w.z), h1.x, a2);
+                a2 = fmaf(bf16_hi(w.z), h1.y, a2);
+                a2 = fmaf(bf16_lo(w.w), h1.z, a2);
+                a2 = fmaf(bf16_hi(w.w), h1.w, a2);
+            }
+            a2 = warp_sum(a2);
+            if (lane == 0) res[r] += gt * a2;
+        }
+        __syncthreads();
+    }
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        float* o = out + (size_t)t * H + r0 + r;
+        *o = accumulate ? (*o + res[r]) : res[r];
+    }
+}
+
+// ====================================================================== shared gate/up
+
+constexpr int kSharedWarps = 4;
+constexpr int kSharedTok = 4;
+
+// grid ceil(S / kSharedWarps) (+1 CTA for the sigmoid gates); block 32 * kSharedWarps.
+// dynamic smem: kSharedTok * H floats.
+__global__ void __launch_bounds__(32 * kSharedWarps) shared_gateup_kernel(const void* __restrict__ x, int x_dtype,
+                                                                          int H, int S, int T,
+                                                                          const uint16_t* __restrict__ wg,
+                                                                          const uint16_t* __restrict__ wu,
+                                                                          const uint16_t* __restrict__ wsig,
+                                                                          float* hs, float* gate) {
+    extern __shared__ __align__(16) float xsf[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_row_ctas = (S + kSharedWarps - 1) / kSharedWarps;
+    const bool gate_cta = (int)blockIdx.x == n_row_ctas;
+    const int r = blockIdx.x * kSharedWarps + warp;
+    for (int t0 = 0; t0 < T; t0 += kSharedTok) {
+        const int nt = min(kSharedTok, T - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * H; i += blockDim.x) xsf[i] = load_x(x, x_dtype, (size_t)t0 * H + i);
+        __syncthreads();
+        if (gate_cta) {
+            for (int tt = warp; tt < nt; tt += kSharedWarps) {
+                const uint4* w4 = reinterpret_cast<const uint4*>(wsig);
+                const float4* x4 = reinterpret_cast<const float4*>(xsf + tt * H);
+                float z = 0.0f;
+                for (int i = lane; i < H / 8; i += 32) {
+                    const uint4 w = __ldg(w4 + i);
+                    const float4 a = x4[2 * i], bb = x4[2 * i + 1];
+                    z = fmaf(bf16_lo(w.x), a.x, z);
+                    z = fmaf(bf16_hi(w.x), a.y, z);
+                    z = fmaf(bf16_lo(w.y), a.z, z);
+                    z = fmaf(bf16_hi(w.y), a.w, z);
+                    z = fmaf(bf16_lo(w.z), bb.x, z);
+                    z = fmaf(bf16_hi(w.z), bb.y, z);
+                    z = fmaf(bf16_lo(w.w), bb.z, z);
+                    z = fmaf(bf16_hi(w.w), bb.w, z);
+                }
+                z = warp_sum(z);
+                if (lane == 0) gate[t0 + tt] = sigmoid(z);
+            }
+            continue;
+        }
+        if (r >= S) continue;
+        float ag[kSharedTok], au[kSharedTok];
+#pragma unroll
+        for (int tt = 0; tt < kSharedTok; tt++) ag[tt] = au[tt] = 0.0f;
+        const uint4* g4 = reinterpret_cast<const uint4*>(wg + (size_t)r * H);
+        const uint4* u4 = reinterpret_cast<const uint4*>(wu + (size_t)r * H);
+        for (int i = lane; i < H / 8; i += 32) {
+            const uint4 gw = __ldg(g4 + i), uw = __ldg(u4 + i);
+#pragma unroll
+            for (int tt = 0; tt < kSharedTok; tt++) {
+                if (tt < nt) {
+                    const float4* x4 = reinterpret_cast<const float4*>(xsf + tt * H);
+                    const float4 a = x4[2 * i], bb = x4[2 * i + 1];
+                    ag[tt] = fmaf(bf16_lo(gw.x), a.x, ag[tt]);
+                    ag[tt] = fmaf(bf16_hi(gw.x), a.y, ag[tt]);
+                    ag[tt] = fmaf(bf16_lo(gw.y), a.z, ag[tt]);
+                    ag[tt] = fmaf(bf16_hi(gw.y), a.w, ag[tt]);
+                    ag[tt] = fmaf(bf16_lo(gw.z), bb.x, ag[tt]);
+                    ag[tt] = fmaf(bf16_hi(gw.z), bb.y, ag[tt]);
+                    ag[tt] = fmaf(bf16_lo(gw.w), bb.z, ag[tt]);
+                    ag[tt] = fmaf(bf16_hi(gw.w), bb.w, ag[tt]);
+                    au[tt] = fmaf(bf16_lo(uw.x), a.x, au[tt]);
+                    au[tt] = fmaf(bf16_hi(uw.x), a.y, au[tt]);
+                    au[tt] = fmaf(bf16_lo(uw.y), a.z, au[tt]);
+                    au[tt] = fmaf(bf16_hi(uw.y), a.w, au[tt]);
+                    au[tt] = fmaf(bf16_lo(uw.z), bb.x, au[tt]);
+                    au[tt] = fmaf(bf16_hi(uw.z), bb.y, au[tt]);
+                    au[tt] = fmaf(bf16_lo(uw.w), bb.z, au[tt]);
+                    au[tt] = fmaf(bf16_hi(uw.w), bb.w, au[tt]);
+                }
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < kSharedTok; tt++) {
+            const float g = warp_sum(ag[tt]), uu = warp_sum(au[tt]);
+            if (lane == 0 && tt < nt) hs[(size_t)(t0 + tt) * S + r] = silu(g) * uu;
+        }
+    }
+}
+
+// ====================================================================== encoder
+
+// One warp per 256-weight block; lane = (sub-block sb = lane/2, half = lane&1).
+// Every integer decision in fp32 with explicit round-to-nearest operations.
+__global__ void __launch_bounds__(256) quantize_kernel(const float* __restrict__ w, int64_t n_blocks,
+                                                       uint8_t* __restrict__ out) {
+    __shared__ uint8_t qbuf[8][256];
+    __shared__ uint8_t sbuf[8][16];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sb = lane >> 1, half = lane & 1;
+    for (int64_t bi = (int64_t)blockIdx.x * 8 + warp; bi < n_blocks; bi += (int64_t)gridDim.x * 8) {
+        const float4* src = reinterpret_cast<const float4*>(w + bi * 256 + 16 * sb + 8 * half);
+        const float4 a = src[0], b = src[1];
+        float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        float mn = v[0], mx = v[0];
+#pragma unroll
+        for (int i = 1; i < 8; i++) {
+            mn = fminf(mn, v[i]);
+            mx = fmaxf(mx, v[i]);
+        }
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        const float m = mn < 0.0f ? -mn : 0.0f;
+        const float s = __fdiv_rn(__fadd_rn(mx, m), 3.0f);
+        const float maxs = warp_max(s);
+        const float maxm = warp_max(m);
+        const __half dh = __float2half_rn(__fdiv_rn(maxs, 15.0f));
+        const __half mh = __float2half_rn(__fdiv_rn(maxm, 15.0f));
+        const float df = __half2float(dh), mf = __half2float(mh);
+        const int lo = df > 0.0f ? (int)fminf(fmaxf(rintf(__fdiv_rn(s, df)), 0.0f), 15.0f) : 0;
+        const int hi = mf > 0.0f ? (int)fminf(fmaxf(rintf(__fdiv_rn(m, mf)), 0.0f), 15.0f) : 0;
+        const float step = __fmul_rn(df, (float)lo);
+        const float base = __fmul_rn(mf, (float)hi);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            int q = 0;
+            if (step > 0.0f) q = (int)fminf(fmaxf(rintf(__fdiv_rn(__fadd_rn(v[i], base), step)), 0.0f), 3.0f);
+            qbuf[warp][16 * sb + 8 * half + i] = (uint8_t)q;
+        }
+        if (half == 0) sbuf[warp][sb] = (uint8_t)(lo | (hi << 4));
+        __syncwarp();
+        uint32_t word = 0;
+        if (lane < 4) {
+            word = (uint32_t)sbuf[warp][4 * lane] | ((uint32_t)sbuf[warp][4 * lane + 1] << 8) |
+                   ((uint32_t)sbuf[warp][4 * lane + 2] << 16) | ((uint32_t)sbuf[warp][4 * lane + 3] << 24);
+        } else if (lane < 20) {
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const int qb = 4 * (lane - 4) + c;  // qs byte 32h + l
+                const int hh = qb >> 5, l = qb & 31;
+                uint32_t byte = 0;
+#pragma unroll
+                for (int j = 0; j < 4; j++) byte |= (uint32_t)qbuf[warp][128 * hh + 32 * j + l] << (2 * j);
+                word |= byte << (8 * c);
+            }
+        } else if (lane == 20) {
+            word = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(mh) << 16);
+        }
+        if (lane < 21) reinterpret_cast<uint32_t*>(out + bi * kBlockBytes)[lane] = word;
+        __syncwarp();
+    }
+}
+
+// ====================================================================== test hook
+
+__global__ void test_wait_kernel(WsHeader* hdr, uint64_t limit_ns) {
+    if (threadIdx.x == 0) wait_geq(&hdr->ctr[kCtrTest][0], 1u, &hdr->status, limit_ns);
+}
+
+// ====================================================================== launchers
+
+static inline size_t align16(size_t v) { return (v + 15) / 16 * 16; }
+
+static cudaError_t set_smem(const void* fn, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t launch_route(const qs_moe_shape& s, const void* x, const float* W, const float* bias, int T,
+                         float* logits, int32_t* ids, float* pw, uint32_t* tickets, cudaStream_t st) {
+    const size_t smem = (size_t)std::min(kRouteTok, T) * s.hidden * sizeof(float);
+    cudaError_t err = set_smem((const void*)route_kernel, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid((s.n_experts + kRouteWarps - 1) / kRouteWarps, (T + kRouteTok - 1) / kRouteTok);
+    route_kernel<<<grid, 32 * kRouteWarps, smem, st>>>(x, s.x_dtype, W, bias, s.hidden, s.n_experts, s.top_k, T,
+                                                       logits, ids, pw, tickets);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group(int E, int k, int T, const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* perm,
+                         cudaStream_t st) {
+    int nw = (12 * 1024 - E - 1) / E;
+    nw = std::max(1, std::min(32, nw));
+    const size_t smem = ((size_t)nw * E + E + 1) * sizeof(int32_t);
+    group_kernel<<<1, 32 * nw, smem, st>>>(ids, T * k, E, counts, offsets, perm);
+    return cudaGetLastError();
+}
+
+static int gemv_rows_per_tile(int rowbytes, int n_streams) {
+    // rows per CTA tile: 16, fewer for long rows so the staged tile stays <= ~48 KB per stream
+    int R = 16;
+    while (R > 4 && (size_t)R * rowbytes * n_streams > 48 * 1024) R >>= 1;
+    return R;
+}
+
+cudaError_t launch_gateup(const qs_moe_shape& s, const void* x, const uint8_t* experts, int64_t stride,
+                          const int32_t* offsets, const int32_t* perm, int T, float* h, cudaStream_t st) {
+    const int H = s.hidden, F = s.expert_ffn;
+    const int rowbytes = H / kBlockWeights * kBlockBytes;
+    const int R = gemv_rows_per_tile(rowbytes, 2);
+    const size_t smem = sizeof(GateUpSmem) + align16((size_t)H * 2) + kGemvThreads * sizeof(float) +
+                        2 * (size_t)R * rowbytes;
+    cudaError_t err = set_smem((const void*)gateup_kernel, smem);
+    if (err != cudaSuccess) return err;
+    const int max_active = std::min(s.n_experts, T * s.top_k);
+    gateup_kernel<<<max_active * (F / R), kGemvThreads, smem, st>>>(x, s.x_dtype, H, s.n_experts, s.top_k, F, R,
+                                                                     experts, stride, offsets, perm, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_down(const qs_moe_shape& s, const uint8_t* experts, int64_t stride, const float* h,
+                        const int32_t* ids, const float* pw, int n_slots, const uint16_t* sh_down,
+                        const float* hs, const float* gate, int T, float* out, int accumulate, cudaStream_t st) {
+    const int H = s.hidden, F = s.expert_ffn;
+    const int rowbytes = F / kBlockWeights * kBlockBytes;
+    const int tpr = 4 * (F / kBlockWeights);
+    const int rows_par = std::max(1, kDownThreads / tpr);
+    int R = std::min(16, 4 * rows_par);  // each thread group handles <= 4 rows
+    while (H % R) R >>= 1;
+    int G = std::max(1, std::min(std::max(n_slots, 1), (int)(96 * 1024 / ((size_t)R * rowbytes + (size_t)F * 2))));
+    const size_t smem = sizeof(DownSmem) + align16((size_t)G * F * 2) + kDownThreads * sizeof(float) +
+                        (size_t)G * R * rowbytes;
+    cudaError_t err = set_smem((const void*)down_kernel, smem);
+    if (err != cudaSuccess) return err;
+    dim3 grid(H / R, T);
+    down_kernel<<<grid, kDownThreads, smem, st>>>(H, s.top_k, F, s.shared_ffn, R, G, experts, stride, h, ids, pw,
+                                                  n_slots, sh_down, hs, gate, out, accumulate);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shared_gateup(const qs_moe_shape& s, const void* x, const uint16_t* wg, const uint16_t* wu,
+                                 const uint16_t* wsig, int T, float* hs, float* gate, cudaStream_t st) {
+    const size_t smem = (size_t)kSharedTok * s.hidden * sizeof(float);
+    cudaError_t err = set_smem((const void*)shared_gateup_kernel, smem);
+    if (err != cudaSuccess) return err;
+    const int grid = (s.shared_ffn + kSharedWarps - 1) / kSharedWarps + 1;
+    shared_gateup_kernel<<<grid, 32 * kSharedWarps, smem, st>>>(x, s.x_dtype, s.hidden, s.shared_ffn, T, wg, wu,
+                                                                wsig, hs, gate);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const float* w, int64_t n_blocks, uint8_t* out, cudaStream_t st) {
+    int64_t grid = (n_blocks + 7) / 8;
+    if (grid > 152 * 64) grid = 152 * 64;
+    quantize_kernel<<<(unsigned)grid, 256, 0, st>>>(w, n_blocks, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_test_wait(void* ws, uint64_t limit_ns, cudaStream_t st) {
+    test_wait_kernel<<<1, 32, 0, st>>>(reinterpret_cast<WsHeader*>(ws), limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace qs

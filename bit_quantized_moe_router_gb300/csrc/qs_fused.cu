@@ -1,0 +1,1151 @@
+// qs_fused.cu -- the whole decode-sized MoE-FFN layer in one persistent kernel (sm_103a).
+//
+// One CTA per SM, launched cooperatively so every CTA is resident.  A CTA has
+// one producer warp and 16 consumer warps.  The producer streams the CTA's
+// tiles from HBM into a ring of 21 KB shared-memory stages with bulk
+// asynchronous copies (TMA engine): one "full" mbarrier per stage counts the
+// bytes in, one "empty" mbarrier per stage tells the producer the stage may
+// be refilled.  Tiles, in the order every CTA walks them (tile i of the grid
+// belongs to CTA i mod gridDim):
+//
+//   router rows (fp32)  |  shared gate/up rows (bf16)  |  routed gate/up rows (Q2_K)  |  down groups
+//
+// Consumers work as independent warp tasks, so different warps can be in
+// different phases at once and nothing waits on a CTA-wide barrier:
+//   group A (warps 0-7):  router rows -> tagged logits; then the routing
+//                         (top-k, softmax, grouping of the T*k entries by expert)
+//   group B (warps 8-15): x scales, int16 x and sigmoid gates; shared gate/up rows -> tagged hs
+//   then every warp, round robin over the CTA's remaining tasks:
+//     routed gate/up rows -> tagged h;  staging of hs and of each entry's int16 h;
+//     down rows: shared-expert down row + every active expert's down row -> out,
+//     summed in a fixed order (ascending expert id, then the gated shared expert)
+//
+// Cross-CTA exchange: logits, hs and h are written as 64-bit words (fp32
+// value | 32-bit call tag) and read by polling the words themselves.  The tag
+// of the last completed call lives in the workspace header; the last CTA to
+// leave advances it.  Every wait is bounded by the global timer; a wait that
+// runs out sets the sticky status QS_ERR_TIMEOUT and the CTA winds down.
+#include "qs_common.cuh"
+#include "qs_internal.h"
+#include "qs_q2k.cuh"
+
+#include <algorithm>
+
+namespace qs {
+
+constexpr int kCW = 16;                  // consumer warps
+constexpr int kCT = kCW * 32;            // consumer threads
+constexpr int kGW = 8;                   // warps per consumer group
+constexpr int kGT = kGW * 32;            // threads per consumer group
+constexpr int kFusedThreads = kCT + 32;  // + the producer warp
+constexpr int kStageBytes = 21504;       // 2 x 128 Q2_K row-blocks of 84 B
+constexpr int kMaxStages = 12;
+constexpr int kMaxEnt = 128;             // T * k
+constexpr int kMaxT = kFusedMaxT;
+constexpr int kMaxCand = 512;            // top-k candidates (per-chunk survivors)
+constexpr int kMaxRD = 16;
+
+struct FusedParams {
+    const void* x;
+    const float* Wr;
+    const float* bias;
+    const uint8_t* experts;
+    int64_t stride;
+    const uint16_t* sg;
+    const uint16_t* su;
+    const uint16_t* sd;
+    const uint16_t* ssig;
+    float* out;
+    uint64_t* xlog;  // [T x E] tagged logits
+    uint64_t* xhs;   // [T x S] tagged hs
+    uint64_t* xh;    // [T*k x F] tagged h
+    WsHeader* hdr;
+    int H, E, k, F, S, T, x_dtype;
+    int RR, RS, R, RD;  // rows per router, shared gate/up, routed gate/up and down tile
+    int nstages;
+    // byte offsets inside the data region that follows FusedCtl
+    int off_xq, off_sig, off_lg, off_hsf, off_hq, off_pbuf, off_stages;
+};
+
+struct alignas(16) FusedCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t xbar;  // x and w_sg
+    int done[kMaxStages];  // tasks finished on the tile now in each stage
+    int slot_seq[kMaxStages];  // sequence number of the tile a stage is being filled with
+    int routed, xq_ready, hs_ready, abort, issued, n_active, shared_left, pad0;
+    uint32_t tag;  // this call's exchange tag
+    int pad[3];
+    int ent_ready[kMaxEnt];
+    int ids[kMaxEnt];
+    float p[kMaxEnt];
+    float lsel[kMaxEnt];
+    int ent_sorted[kMaxEnt];     // entries t*k+slot sorted by (expert, entry)
+    int es[kMaxEnt];             // expert of ent_sorted[i]
+    int act_e[kMaxEnt];          // active experts, ascending
+    int act_begin[kMaxEnt + 1];  // first ent_sorted index of each active expert
+    int tok_sorted[kMaxEnt];     // per token, its k ent_sorted indices, ascending
+    int wcnt[8];
+    float gate_s[kMaxT];
+    float xscale[kMaxT];
+    float hscale[kMaxEnt];
+    float red[2 * kGT];
+    float cand_v[kMaxCand];
+    int cand_i[kMaxCand];
+};
+
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGT) : "memory"); }
+
+// number of threads of consumer group `id` whose predicate is true (a group barrier)
+__device__ __forceinline__ int group_count(int id, bool pred) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %2, 0;\n\t"
+        "bar.red.popc.u32 %0, %1, %3, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"((int)pred), "n"(kGT)
+        : "memory");
+    return r;
+}
+
+__device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+__device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
+
+__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+__device__ __forceinline__ float tag_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+
+// ------------------------------------------------------------------ tile and task bookkeeping
+
+struct Plan {
+    int G, cta;
+    int n_rt, n_st, n_ind;    // router tiles, shared gate/up tiles, routing-independent total
+    int tpe;                  // routed gate/up tiles per active expert
+    int n_dg;                 // down groups
+    int rowH, rowF;           // Q2_K row bytes along H and along F
+    int bs, be;               // bytes of a down group's shared part / one expert's down rows
+    int m0, mf;               // experts in the first / in a further down sub-tile
+    int own_rt, own_st;       // tiles of each kind this CTA owns
+    int cpr, rpw, ept;        // Q2_K chunks per gate/up row, rows per task, tasks per tile
+    int cpf, epp;             // chunks per down row, experts per warp pass
+};
+
+__device__ __forceinline__ int first_owned(int lo, int G, int cta) {
+    const int r = lo % G;
+    return lo + ((cta - r) % G + G) % G;
+}
+__device__ __forceinline__ int owned_count(int lo, int hi, int G, int cta) {
+    const int f = first_owned(lo, G, cta);
+    return f < hi ? (hi - 1 - f) / G + 1 : 0;
+}
+
+__device__ __forceinline__ Plan make_plan(const FusedParams& P) {
+    Plan L;
+    L.G = gridDim.x;
+    L.cta = blockIdx.x;
+    L.n_rt = P.E / P.RR;
+    L.n_st = P.S > 0 ? P.S / P.RS : 0;
+    L.n_ind = L.n_rt + L.n_st;
+    L.tpe = P.F / P.R;
+    L.n_dg = P.H / P.RD;
+    L.rowH = P.H / kBlockWeights * kBlockBytes;
+    L.rowF = P.F / kBlockWeights * kBlockBytes;
+    L.bs = P.S > 0 ? P.RD * P.S * 2 : 0;
+    L.be = P.RD * L.rowF;
+    L.m0 = (kStageBytes - L.bs) / L.be;
+    L.mf = kStageBytes / L.be;
+    L.own_rt = owned_count(0, L.n_rt, L.G, L.cta);
+    L.own_st = owned_count(L.n_rt, L.n_ind, L.G, L.cta);
+    L.cpr = 4 * (P.H / kBlockWeights);
+    L.rpw = L.cpr >= 32 ? 1 : 32 / L.cpr;
+    L.ept = P.R / L.rpw;
+    L.cpf = 4 * (P.F / kBlockWeights);
+    L.epp = 32 / L.cpf;
+    return L;
+}
+
+__device__ __forceinline__ int down_subtiles(int n_active, const Plan& L) {
+    const int rest = n_active - L.m0;
+    return 1 + (rest > 0 ? (rest + L.mf - 1) / L.mf : 0);
+}
+
+// expert range [a0, a1) of down sub-tile s
+__device__ __forceinline__ void down_sub_range(int s, int n_active, const Plan& L, int& a0, int& a1) {
+    if (s == 0) {
+        a0 = 0;
+        a1 = min(n_active, L.m0);
+    } else {
+        a0 = L.m0 + (s - 1) * L.mf;
+        a1 = min(n_active, a0 + L.mf);
+    }
+}
+
+// ------------------------------------------------------------------ waits (bounded, warp-uniform outcome)
+
+// Whole warp waits for an mbarrier phase; false if any lane gave up or the CTA is aborting.
+__device__ __forceinline__ bool warp_wait_bar(FusedCtl& C, uint64_t* bar, uint32_t parity) {
+    const bool ok = !vload(&C.abort) && mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Whole warp waits for tile `seq` in its stage.  A warp may run laps ahead of the
+// producer, so it first waits until the stage is being filled with this very
+// tile (parity alone cannot tell laps apart), then for the stage's bytes.
+__device__ __forceinline__ bool warp_wait_tile(FusedCtl& C, int seq, int ns) {
+    const int slot = seq % ns;
+    bool ok = true;
+    if (vload(&C.slot_seq[slot]) != seq) {
+        const uint64_t t0 = global_timer_ns();
+        while (vload(&C.slot_seq[slot]) != seq) {
+            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    ok = ok && !vload(&C.abort) && mbar_wait(&C.full[slot], (seq / ns) & 1);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Whole warp waits until *v == 0 (shared memory); false on abort or time-out.
+__device__ __forceinline__ bool warp_wait_zero(FusedCtl& C, const int* v) {
+    bool ok = true;
+    if (vload(v) != 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (vload(v) != 0) {
+            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Whole warp waits until *flag != 0 (shared memory); false on abort or time-out.
+__device__ __forceinline__ bool warp_wait_flag(FusedCtl& C, const int* flag) {
+    bool ok = true;
+    if (!vload(flag)) {
+        const uint64_t t0 = global_timer_ns();
+        while (!vload(flag)) {
+            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ void fail(FusedCtl& C, uint32_t* status) {
+    if ((threadIdx.x & 31) == 0) {
+        set_status(status, QS_ERR_TIMEOUT);
+        vstore(&C.abort, 1);
+    }
+}
+
+// A task is done with the tile in stage `slot` (ntask tasks share it): the last
+// one hands the stage back to the producer.
+__device__ __forceinline__ void release_slot(FusedCtl& C, int slot, int ntask) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+        if (atomicAdd(&C.done[slot], 1) == ntask - 1) {
+            C.done[slot] = 0;
+            mbar_arrive(&C.empty[slot]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ producer warp
+
+// lane 0 waits until stage seq % ns is free (bounded), then marks it as holding
+// tile seq; outcome broadcast to the warp
+__device__ __forceinline__ bool producer_slot(FusedCtl& C, int seq, int ns) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        if (seq >= ns) {
+            ok = (!vload(&C.abort) && mbar_wait(&C.empty[seq % ns], (seq / ns - 1) & 1)) ? 1 : 0;
+            if (!ok) vstore(&C.abort, 1);
+        }
+        if (ok) vstore(&C.slot_seq[seq % ns], seq);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
+    const Plan L = make_plan(P);
+    const int lane = threadIdx.x & 31;
+    const int ns = P.nstages;
+    uint8_t* stages = data + P.off_stages;
+    int seq = 0;
+    auto slot = [&](int s) { return stages + (size_t)(s % ns) * kStageBytes; };
+    auto bar = [&](int s) { return &C.full[s % ns]; };
+
+    // x and the shared-expert gate vector first: group A and group B start on them
+    {
+        const uint32_t xb = (uint32_t)P.T * P.H * (P.x_dtype == QS_BF16 ? 2 : 4);
+        const uint32_t sb = P.S > 0 ? (uint32_t)P.H * 2 : 0u;
+        if (lane == 0) mbar_arrive_expect_tx(&C.xbar, xb + sb);
+        __syncwarp();
+        if (lane == 0) bulk_g2s(data, P.x, xb, &C.xbar);
+        if (lane == 1 && sb) bulk_g2s(data + P.off_sig, P.ssig, sb, &C.xbar);
+    }
+    // router rows, then shared gate/up rows
+#pragma unroll 1
+    for (int g = L.cta; g < L.n_ind; g += L.G) {
+        if (!producer_slot(C, seq, ns)) goto done;
+        if (g < L.n_rt) {
+            const uint32_t bytes = (uint32_t)P.RR * P.H * 4;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(seq), bytes);
+                fence_proxy_async_smem();
+                bulk_g2s(slot(seq), P.Wr + (size_t)g * P.RR * P.H, bytes, bar(seq));
+            }
+        } else {
+            const int j = g - L.n_rt;
+            const uint32_t bytes = (uint32_t)P.RS * P.H * 2;
+            if (lane == 0) mbar_arrive_expect_tx(bar(seq), 2 * bytes);
+            __syncwarp();
+            if (lane < 2) {
+                fence_proxy_async_smem();
+                bulk_g2s(slot(seq) + lane * bytes, (lane ? P.su : P.sg) + (size_t)j * P.RS * P.H, bytes, bar(seq));
+            }
+        }
+        __syncwarp();
+        seq++;
+    }
+    // the routing, published by group A
+    if (!warp_wait_flag(C, &C.routed)) {
+        if (lane == 0) vstore(&C.abort, 1);
+        goto done;
+    }
+    __threadfence_block();
+    {
+        const int na = C.n_active;
+        const int n_et = na * L.tpe;
+        const int lo_dg = L.n_ind + n_et, hi_dg = lo_dg + L.n_dg;
+        const int64_t down_off = 2ll * P.F * L.rowH;
+        // routed gate/up rows: the critical path, issued first
+#pragma unroll 1
+        for (int g = first_owned(L.n_ind, L.G, L.cta); g < L.n_ind + n_et; g += L.G) {
+            if (!producer_slot(C, seq, ns)) goto done;
+            const int idx = g - L.n_ind;
+            const int a = idx / L.tpe, tt = idx % L.tpe;
+            const uint8_t* gate = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)tt * P.R * L.rowH;
+            const uint32_t bytes = (uint32_t)P.R * L.rowH;
+            if (lane == 0) mbar_arrive_expect_tx(bar(seq), 2 * bytes);
+            __syncwarp();
+            if (lane < 2) {
+                fence_proxy_async_smem();
+                bulk_g2s(slot(seq) + lane * bytes, gate + (int64_t)lane * P.F * L.rowH, bytes, bar(seq));
+            }
+            __syncwarp();
+            seq++;
+        }
+        // down groups: nsub consecutive stages each
+        const int nsub = down_subtiles(na, L);
+#pragma unroll 1
+        for (int g = first_owned(lo_dg, L.G, L.cta); g < hi_dg; g += L.G) {
+            const int r0 = (g - lo_dg) * P.RD;
+#pragma unroll 1
+            for (int s = 0; s < nsub; s++) {
+                if (!producer_slot(C, seq, ns)) goto done;
+                int a0, a1;
+                down_sub_range(s, na, L, a0, a1);
+                const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+                if (lane == 0) mbar_arrive_expect_tx(bar(seq), sh + (uint32_t)(a1 - a0) * L.be);
+                __syncwarp();
+                // copy c = 0 is the shared part (sub-tile 0 only), c >= 1 the experts
+#pragma unroll 1
+                for (int c = lane; c < 1 + (a1 - a0); c += 32) {
+                    fence_proxy_async_smem();
+                    if (c == 0) {
+                        if (sh) bulk_g2s(slot(seq), P.sd + (size_t)r0 * P.S, sh, bar(seq));
+                    } else {
+                        const int a = a0 + c - 1;
+                        bulk_g2s(slot(seq) + sh + (size_t)(c - 1) * L.be,
+                                 P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF,
+                                 (uint32_t)L.be, bar(seq));
+                    }
+                }
+                __syncwarp();
+                seq++;
+            }
+        }
+    }
+done:
+    if (lane == 0) vstore(&C.issued, seq);
+}
+
+// ------------------------------------------------------------------ warp-level arithmetic
+
+__device__ __forceinline__ void load8(const uint8_t* p, bool f32, float* v) {
+    if (f32) {
+        const float4 a = reinterpret_cast<const float4*>(p)[0];
+        const float4 b = reinterpret_cast<const float4*>(p)[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+        v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+        v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    }
+}
+
+// One warp: dot products of one dense row (K elements, fp32 or bf16, shared
+// memory) with T activation rows (fp32 or bf16, shared memory), lane-strided by
+// 8 elements, then summed over the warp.  Every lane gets acc[t].
+template <int MAXT>
+__device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int K, const uint8_t* act, bool a_f32,
+                                               int T, float* acc) {
+    const int lane = threadIdx.x & 31;
+    const int wsz = w_f32 ? 4 : 2, asz = a_f32 ? 4 : 2;
+#pragma unroll
+    for (int t = 0; t < MAXT; t++) acc[t] = 0.0f;
+#pragma unroll 1
+    for (int i = lane * 8; i < K; i += 256) {
+        float wv[8];
+        load8(w + (size_t)i * wsz, w_f32, wv);
+#pragma unroll
+        for (int t = 0; t < MAXT; t++) {
+            if (t < T) {
+                float av[8];
+                load8(act + ((size_t)t * K + i) * asz, a_f32, av);
+                float s = acc[t];
+#pragma unroll
+                for (int q = 0; q < 8; q++) s = fmaf(wv[q], av[q], s);
+                acc[t] = s;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MAXT; t++)
+        if (t < T) acc[t] = warp_sum(acc[t]);
+}
+
+// key order of the top-k: larger logit first, then the lower expert id
+__device__ __forceinline__ bool key_before(float v, int i, float ov, int oi) { return v > ov || (v == ov && i < oi); }
+
+// Sort 32 (value, index) pairs held one per lane into key order (bitonic network).
+__device__ __forceinline__ void warp_sort32(float& v, int& i) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
+            const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
+            const bool first = (lane & size) == 0 || size == 32;  // this block ends up in key order
+            const bool lower = (lane & stride) == 0;
+            const bool mine_first = key_before(v, i, ov, oi);
+            if ((lower == first) ? !mine_first : mine_first) {
+                v = ov;
+                i = oi;
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <int MAXT>
+__global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const FusedParams P) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    FusedCtl& C = *reinterpret_cast<FusedCtl*>(smem);
+    uint8_t* data = smem + (sizeof(FusedCtl) + 127) / 128 * 128;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = P.H, E = P.E, k = P.k, F = P.F, S = P.S, T = P.T;
+    const int n_ent = T * k;
+    const bool x_f32 = P.x_dtype != QS_BF16;
+    uint32_t* status = &P.hdr->status;
+    uint32_t* ctr_exit = &P.hdr->ctr[kCtrExit][0];
+    uint32_t* epoch = &P.hdr->ctr[kCtrEpoch][0];
+    const uint8_t* xraw = data;                                              // [T x H] as given
+    uint32_t* xqf = reinterpret_cast<uint32_t*>(data + P.off_xq);            // [T][H/64 chunks][36] fragments
+    const uint8_t* sigbuf = data + P.off_sig;                                // [H] bf16
+    float* lg = reinterpret_cast<float*>(data + P.off_lg);                   // [T x E]
+    float* hsf = reinterpret_cast<float*>(data + P.off_hsf);                 // [T x S]
+    uint32_t* hqf = reinterpret_cast<uint32_t*>(data + P.off_hq);            // [T*k][F/64 chunks][36] fragments
+    float* pbuf = reinterpret_cast<float*>(data + P.off_pbuf);               // [16 warps x kMaxEnt]
+    uint8_t* stages = data + P.off_stages;
+    const int ns = P.nstages;
+
+    if (tid == 0) {
+        for (int i = 0; i < ns; i++) {
+            mbar_init(&C.full[i], 1);
+            mbar_init(&C.empty[i], 1);
+            C.done[i] = 0;
+            C.slot_seq[i] = -1;
+        }
+        mbar_init(&C.xbar, 1);
+        C.routed = C.xq_ready = C.hs_ready = C.abort = C.issued = C.n_active = 0;
+        {
+            const Plan L0 = make_plan(P);
+            C.shared_left = L0.own_st * P.RS;  // shared gate/up row tasks of this CTA
+        }
+        fence_barrier_init();
+    }
+#pragma unroll 1
+    for (int i = tid; i < kMaxEnt; i += blockDim.x) C.ent_ready[i] = 0;
+    __syncthreads();
+
+    if (warp == kCW) {
+        producer(P, C, data);
+    } else {
+        const Plan L = make_plan(P);
+        // this call's exchange tag: one past the epoch the previous call left (never 0)
+        uint32_t tag = 0;
+        if (lane == 0) {
+            tag = ld_acquire(epoch) + 1u;
+            if (tag == 0) tag = 1u;
+            if (warp == 0) C.tag = tag;
+        }
+        tag = __shfl_sync(0xffffffffu, tag, 0);
+        const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
+        bool ok = warp_wait_bar(C, &C.xbar, 0);
+        if (!ok) fail(C, status);
+
+        if (warp < kGW) {
+            // ------------------------------------------------------ group A: router rows
+#pragma unroll 1
+            for (int idx = gwarp; ok && idx < L.own_rt * P.RR; idx += kGW) {
+                const int m = idx / P.RR, r = idx % P.RR;
+                const int g = L.cta + m * L.G;
+                if (!(ok = warp_wait_tile(C, m, ns))) break;
+                float acc[MAXT];
+                warp_dense_row<MAXT>(stages + (size_t)(m % ns) * kStageBytes + (size_t)r * H * 4, true, H, xraw, x_f32,
+                                     T, acc);
+                const int e = g * P.RR + r;
+                const float b = P.bias ? P.bias[e] : 0.0f;
+#pragma unroll
+                for (int t = 0; t < MAXT; t++)
+                    if (t < T && lane == t) st_tagged(P.xlog + (size_t)t * E + e, acc[t] + b, tag);
+                release_slot(C, m % ns, P.RR);
+            }
+            if (!ok) fail(C, status);
+            // ------------------------------------------------------ group A: routing
+            // group-uniform outcome of the previous waits
+            ok = group_count(2, !ok) == 0;
+            if (ok) {
+                const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+                for (;;) {
+                    bool mine = true;
+#pragma unroll 1
+                    for (int i = gtid; i < T * E; i += kGT) {
+                        const uint64_t w = ld_tagged(P.xlog + i);
+                        mine &= tag_ok(w, tag);
+                        const float v = tag_value(w);
+                        lg[i] = (v == v) ? v : -INFINITY;  // a NaN logit ranks last
+                    }
+                    if (group_count(2, !mine) == 0) break;
+                    const bool late = gtid == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs);
+                    if (group_count(2, late) > 0) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (ok) {
+                // per 32-logit chunk: sort, keep the first k as candidates
+                const int chunks = (E + 31) / 32;
+                const int kc = min(k, 32);
+#pragma unroll 1
+                for (int q = gwarp; q < T * chunks; q += kGW) {
+                    const int t = q / chunks, ch = q % chunks;
+                    const int e = ch * 32 + lane;
+                    float v = e < E ? lg[t * E + e] : -INFINITY;
+                    int i = e < E ? e : 0x7fffffff;
+                    warp_sort32(v, i);
+                    if (lane < kc) {
+                        C.cand_v[q * kc + lane] = v;
+                        C.cand_i[q * kc + lane] = i;
+                    }
+                }
+                group_sync(2);
+                // rank among the token's candidates: rank < k is selected
+                const int nc = chunks * kc;
+#pragma unroll 1
+                for (int q = gtid; q < T * nc; q += kGT) {
+                    const int t = q / nc;
+                    const float v = C.cand_v[q];
+                    const int i = C.cand_i[q];
+                    int rank = 0;
+#pragma unroll 1
+                    for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
+                    if (rank < k && i < E) {
+                        C.ids[t * k + rank] = i;
+                        C.lsel[t * k + rank] = v;
+                    }
+                }
+                group_sync(2);
+                // softmax over the selected logits (one warp per token)
+#pragma unroll 1
+                for (int t = gwarp; t < T; t += kGW) {
+                    const float l0 = C.lsel[t * k];
+                    float ex = 0.0f;
+#pragma unroll 1
+                    for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
+                    const float den = warp_sum(ex);
+#pragma unroll 1
+                    for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
+                }
+                // order the entries by (expert, entry)
+#pragma unroll 1
+                for (int i = gtid; i < n_ent; i += kGT) {
+                    const int e = C.ids[i];
+                    int rank = 0;
+#pragma unroll 1
+                    for (int j = 0; j < n_ent; j++) {
+                        const int f = C.ids[j];
+                        rank += (f < e) || (f == e && j < i);
+                    }
+                    C.ent_sorted[rank] = i;
+                    C.es[rank] = e;
+                }
+                group_sync(2);
+                // active experts: a run start in es[] opens a new active expert
+                const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
+                const unsigned bal = __ballot_sync(0xffffffffu, start);
+                if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
+                group_sync(2);
+                if (gtid < n_ent) {
+                    int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+#pragma unroll 1
+                    for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
+                    if (start) {
+                        C.act_e[a] = C.es[gtid];
+                        C.act_begin[a] = gtid;
+                    }
+                    if (gtid == n_ent - 1) {
+                        C.act_begin[a + 1] = n_ent;
+                        C.n_active = a + 1;
+                    }
+                    const int t = C.ent_sorted[gtid] / k;
+                    int pos = 0;
+#pragma unroll 1
+                    for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
+                    C.tok_sorted[t * k + pos] = gtid;
+                }
+                group_sync(2);
+                if (gtid == 0) {
+                    __threadfence_block();
+                    vstore(&C.routed, 1);
+                }
+            } else {
+                fail(C, status);
+            }
+        } else {
+            // ------------------------------------------------------ group B: x scales, int16 x, gates
+            ok = group_count(3, !ok) == 0;
+            if (ok) {
+                float mx[MAXT], gz[MAXT];
+#pragma unroll
+                for (int t = 0; t < MAXT; t++) mx[t] = gz[t] = 0.0f;
+#pragma unroll 1
+                for (int i = gtid * 8; i < H; i += kGT * 8) {
+                    float sv[8];
+                    if (S > 0) load8(sigbuf + (size_t)i * 2, false, sv);
+#pragma unroll
+                    for (int t = 0; t < MAXT; t++) {
+                        if (t < T) {
+                            float xv[8];
+                            load8(xraw + ((size_t)t * H + i) * (x_f32 ? 4 : 2), x_f32, xv);
+#pragma unroll
+                            for (int q = 0; q < 8; q++) {
+                                mx[t] = fmaxf(mx[t], fabsf(xv[q]));
+                                if (S > 0) gz[t] = fmaf(sv[q], xv[q], gz[t]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < MAXT; t++) {
+                    if (t < T) {
+                        const float m = warp_max(mx[t]);
+                        const float z = warp_sum(gz[t]);
+                        if (lane == 0) {
+                            C.red[gwarp * MAXT + t] = m;
+                            C.red[kGT + gwarp * MAXT + t] = z;
+                        }
+                    }
+                }
+                group_sync(3);
+                if (gtid < T) {
+                    float m = 0.0f, z = 0.0f;
+#pragma unroll 1
+                    for (int w = 0; w < kGW; w++) {
+                        m = fmaxf(m, C.red[w * MAXT + gtid]);
+                        z += C.red[kGT + w * MAXT + gtid];
+                    }
+                    C.xscale[gtid] = m;
+                    C.gate_s[gtid] = sigmoid(z);
+                }
+                group_sync(3);
+                // int16 x in fragment layout; each 8-value group is one 16-byte store, the
+                // two groups of a 16-value shift group are adjacent lanes (sums via shuffle)
+#pragma unroll 1
+                for (int i0 = gtid * 8; i0 < ((T * H + 255) / 256) * 256; i0 += kGT * 8) {
+                    const bool live = i0 < T * H;
+                    const int t = live ? i0 / H : 0, p = live ? i0 - t * H : 0;
+                    const float m = C.xscale[t];
+                    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+                    float xv[8];
+                    if (live) load8(xraw + (size_t)i0 * (x_f32 ? 4 : 2), x_f32, xv);
+                    uint32_t wq[4];
+                    int sum = 0;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const int a0 = live ? __float2int_rn(xv[2 * q] * inv) : 0;
+                        const int a1 = live ? __float2int_rn(xv[2 * q + 1] * inv) : 0;
+                        wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
+                        sum += a0 + a1;
+                    }
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    if (live) {
+                        int word, half;
+                        frag_pos(p, word, half);
+                        uint32_t* row = xqf + (size_t)t * (H / 64) * kFragWords;
+                        *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
+                    }
+                }
+                group_sync(3);
+                if (gtid == 0) {
+                    __threadfence_block();
+                    vstore(&C.xq_ready, 1);
+                }
+            } else {
+                fail(C, status);
+            }
+            // ------------------------------------------------------ group B: shared gate/up rows
+#pragma unroll 1
+            for (int idx = gwarp; ok && idx < L.own_st * P.RS; idx += kGW) {
+                const int m = idx / P.RS, r = idx % P.RS;
+                const int sq = L.own_rt + m;
+                const int j = first_owned(L.n_rt, L.G, L.cta) + m * L.G - L.n_rt;
+                if (!(ok = warp_wait_tile(C, sq, ns))) break;
+                const uint8_t* st = stages + (size_t)(sq % ns) * kStageBytes;
+                float ga[MAXT], ua[MAXT];
+                warp_dense_row<MAXT>(st + (size_t)r * H * 2, false, H, xraw, x_f32, T, ga);
+                warp_dense_row<MAXT>(st + (size_t)(P.RS + r) * H * 2, false, H, xraw, x_f32, T, ua);
+#pragma unroll
+                for (int t = 0; t < MAXT; t++)
+                    if (t < T && lane == t) st_tagged(P.xhs + (size_t)t * S + j * P.RS + r, silu(ga[t]) * ua[t], tag);
+                release_slot(C, sq % ns, P.RS);
+                if (lane == 0) atomicSub(&C.shared_left, 1);
+            }
+            if (!ok) fail(C, status);
+        }
+
+        // ---------------------------------------------------------- every warp: the routed part
+        if (ok && !(ok = warp_wait_flag(C, &C.routed))) fail(C, status);
+        __threadfence_block();
+        const int na = ok ? C.n_active : 0;
+        const int n_et = na * L.tpe;
+        const int own_et = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta);
+        const int lo_dg = L.n_ind + n_et;
+        const int own_dg = owned_count(lo_dg, lo_dg + L.n_dg, L.G, L.cta);
+        const int nsub = down_subtiles(na, L);
+        const int seq_et = L.own_rt + L.own_st;       // stage sequence number of the first routed tile
+        const int seq_dg = seq_et + own_et;           // ... of the first down group
+        const int n_stage_tasks = (S > 0 ? 1 : 0) + n_ent;
+        const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
+        const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
+        bool xq_seen = false;
+#pragma unroll 1
+        for (int q = warp; ok && q < q_all; q += kCW) {
+            if (q < q_et) {
+                // ---------------------------------------------- routed gate/up rows
+                if (!xq_seen) {
+                    if (!(ok = warp_wait_flag(C, &C.xq_ready))) break;
+                    __threadfence_block();
+                    xq_seen = true;
+                }
+                const int m = q / L.ept, rt = q % L.ept;
+                const int sq = seq_et + m;
+                const int g = first_owned(L.n_ind, L.G, L.cta) + m * L.G;
+                const int idx = g - L.n_ind;
+                const int a = idx / L.tpe, tt = idx % L.tpe;
+                if (!(ok = warp_wait_tile(C, sq, ns))) break;
+                const uint8_t* st = stages + (size_t)(sq % ns) * kStageBytes;
+                // lanes: (row within the task, chunk); long rows: each lane walks several chunks
+                const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
+                const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
+                const int cstep = L.cpr >= 32 ? 32 : L.cpr;
+                const int r = rt * L.rpw + rl;
+                const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
+#pragma unroll 1
+                for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                    const int ent = C.ent_sorted[j];
+                    const int t = ent / k;
+                    float gv = 0.0f, uv = 0.0f;
+#pragma unroll 1
+                    for (int c = c0; c < L.cpr; c += cstep) {
+                        const int b = c >> 2, u = c & 3;
+                        XFrag f;
+                        load_xfrag_f(xqf + ((size_t)t * (H / 64) + c) * kFragWords, f);
+                        const uint8_t* grow = st + (size_t)r * L.rowH + b * kBlockBytes;
+                        gv += q2k_chunk_dot(grow, u, f);
+                        uv += q2k_chunk_dot(grow + (size_t)P.R * L.rowH, u, f);
+                    }
+                    for (int o = min(L.cpr, 32) >> 1; o > 0; o >>= 1) {
+                        gv += __shfl_xor_sync(gm, gv, o);
+                        uv += __shfl_xor_sync(gm, uv, o);
+                    }
+                    if (c0 == 0) {
+                        const float sx = C.xscale[t] * (1.0f / 32767.0f);
+                        st_tagged(P.xh + (size_t)ent * F + tt * P.R + r, silu(gv * sx) * (uv * sx), tag);
+                    }
+                }
+                release_slot(C, sq % ns, L.ept);
+            } else if (q < q_et + n_stage_tasks) {
+                // ---------------------------------------------- staging of hs / of one entry's int16 h
+                const int sidx = q - q_et;
+                // the int16 h cache aliases x, w_sg and the logits: wait until their last reader is done
+                if (!(ok = warp_wait_flag(C, &C.xq_ready))) break;
+                if (!(ok = warp_wait_zero(C, &C.shared_left))) break;
+                __threadfence_block();
+                const uint64_t t0 = global_timer_ns();
+                if (S > 0 && sidx == 0) {
+#pragma unroll 1
+                    for (;;) {
+                        bool mine = true;
+#pragma unroll 1
+                        for (int i = lane; i < T * S; i += 32) {
+                            const uint64_t w = ld_tagged(P.xhs + i);
+                            mine &= tag_ok(w, tag);
+                            hsf[i] = tag_value(w);
+                        }
+                        if (__all_sync(0xffffffffu, mine)) break;
+                        if (__any_sync(0xffffffffu, lane == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs))) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence_block();
+                        vstore(&C.hs_ready, 1);
+                    }
+                } else {
+                    const int ent = sidx - (S > 0 ? 1 : 0);
+                    const uint64_t* hr = P.xh + (size_t)ent * F;
+                    float m;
+#pragma unroll 1
+                    for (;;) {
+                        bool mine = true;
+                        m = 0.0f;
+#pragma unroll 1
+                        for (int i = lane; i < F; i += 32) {
+                            const uint64_t w = ld_tagged(hr + i);
+                            mine &= tag_ok(w, tag);
+                            m = fmaxf(m, fabsf(tag_value(w)));
+                        }
+                        if (__all_sync(0xffffffffu, mine)) break;
+                        if (__any_sync(0xffffffffu, lane == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs))) {
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (!ok) break;
+                    m = warp_max(m);
+                    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+                    uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
+#pragma unroll 1
+                    for (int p = lane * 8; p < F; p += 256) {
+                        uint32_t wq[4];
+                        int sum = 0;
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            const int a0 = __float2int_rn(tag_value(ld_tagged(hr + p + 2 * q)) * inv);
+                            const int a1 = __float2int_rn(tag_value(ld_tagged(hr + p + 2 * q + 1)) * inv);
+                            wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
+                            sum += a0 + a1;
+                        }
+                        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                        int word, half;
+                        frag_pos(p, word, half);
+                        *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                        if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
+                    }
+                    if (lane == 0) C.hscale[ent] = m * (1.0f / 32767.0f);
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence_block();
+                        vstore(&C.ent_ready[ent], 1);
+                    }
+                }
+            } else {
+                // ---------------------------------------------- one down row
+                const int dq = q - q_et - n_stage_tasks;
+                const int m = dq / P.RD, r = dq % P.RD;
+                const int g = first_owned(lo_dg, L.G, L.cta) + m * L.G;
+                const int r0 = (g - lo_dg) * P.RD;
+                const int sq0 = seq_dg + m * nsub;
+#pragma unroll 1
+                for (int s = 0; ok && s < nsub; s++) ok = warp_wait_tile(C, sq0 + s, ns);
+                if (ok && S > 0) ok = warp_wait_flag(C, &C.hs_ready);
+#pragma unroll 1
+                for (int e2 = 0; ok && e2 < n_ent; e2++) ok = warp_wait_flag(C, &C.ent_ready[e2]);
+                if (!ok) break;
+                __threadfence_block();
+                float* pb = pbuf + warp * kMaxEnt;
+                // routed experts: epp experts per pass, cpf lanes per expert row
+                const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
+                const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
+                const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
+#pragma unroll 1
+                for (int s = 0; s < nsub; s++) {
+                    const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
+                    int a0, a1;
+                    down_sub_range(s, na, L, a0, a1);
+                    const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+#pragma unroll 1
+                    for (int pa = a0; pa < a1; pa += L.epp) {
+                        const int a = pa + al;
+                        if (a < a1) {
+                            const int b = c0 >> 2, u = c0 & 3;
+                            const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
+#pragma unroll 1
+                            for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                                const int ent = C.ent_sorted[j];
+                                XFrag f;
+                                load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
+                                float v = q2k_chunk_dot(row, u, f);
+                                for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
+                                if (c0 == 0) pb[j] = v * C.hscale[ent];
+                            }
+                        }
+                    }
+                }
+                // shared expert down row
+                float sacc[MAXT];
+                if (S > 0)
+                    warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
+                                         reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
+                __syncwarp();
+#pragma unroll
+                for (int t = 0; t < MAXT; t++) {
+                    if (t < T && lane == t) {
+                        float acc = 0.0f;
+#pragma unroll 1
+                        for (int mm = 0; mm < k; mm++) {
+                            const int j = C.tok_sorted[t * k + mm];
+                            acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
+                        }
+                        if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
+                        P.out[(size_t)t * H + r0 + r] = acc;
+                    }
+                }
+#pragma unroll 1
+                for (int s = 0; s < nsub; s++) release_slot(C, (sq0 + s) % ns, P.RD);
+            }
+        }
+        if (!ok) fail(C, status);
+    }
+
+    __syncthreads();
+    if (tid == 0) {
+        // never leave a copy in flight into shared memory that is about to be released
+        const int issued = vload(&C.issued);
+#pragma unroll 1
+        for (int s = max(0, issued - ns); s < issued; s++)
+            if (!mbar_wait(&C.full[s % ns], (s / ns) & 1)) set_status(status, QS_ERR_TIMEOUT);
+        if (!mbar_wait(&C.xbar, 0)) set_status(status, QS_ERR_TIMEOUT);
+        if (vload(&C.abort)) set_status(status, QS_ERR_TIMEOUT);
+        const uint32_t old = atom_acq_rel_add(ctr_exit, 1u);
+        if (old == gridDim.x - 1) {
+            // last CTA out: every tagged word of this call has been read; advance the epoch
+            *reinterpret_cast<volatile uint32_t*>(ctr_exit) = 0u;
+            *reinterpret_cast<volatile uint32_t*>(epoch) = C.tag;
+            __threadfence();
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+static bool pow2(int v) { return v > 0 && (v & (v - 1)) == 0; }
+static size_t up16(size_t v) { return (v + 15) / 16 * 16; }
+
+struct FusedPlanHost {
+    int RR, RS, R, RD, nstages;
+    int off_xq, off_sig, off_lg, off_hsf, off_hq, off_pbuf, off_stages;
+    size_t smem;
+};
+
+static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, FusedPlanHost& fp) {
+    const int H = s.hidden, E = s.n_experts, k = s.top_k, F = s.expert_ffn, S = s.shared_ffn;
+    const int nbH = H / 256, nbF = F / 256;
+    const int xsz = s.x_dtype == QS_BF16 ? 2 : 4;
+    if (T < 1 || T > kMaxT || T * k > kMaxEnt || T > 32) return false;
+    if (T * ((E + 31) / 32) * std::min(k, 32) > kMaxCand) return false;
+    if (!pow2(nbH) || nbH > 32 || !pow2(nbF) || 4 * nbF > 32) return false;
+    if (S > 0 && (!pow2(S / 256) || S / 256 > 32)) return false;
+    if (H * 4 > kStageBytes) return false;            // a router row must fit a stage
+    if (S > 0 && 4 * H > kStageBytes) return false;    // a shared gate+up row pair must fit
+    fp.RR = std::min(E, kStageBytes / (H * 4));
+    while (E % fp.RR) fp.RR--;
+    fp.RS = 0;
+    if (S > 0) {
+        fp.RS = kStageBytes / (4 * H);
+        while (S % fp.RS) fp.RS--;
+    }
+    fp.R = 128 / nbH;
+    const int rowF = nbF * 84;
+    const int rd_align = 4 / std::min(nbF, 4);
+    const int na_max = std::min(E, T * k);
+    int RD = kMaxRD;
+    while (RD > rd_align && (RD * (2 * S + na_max * rowF) > kStageBytes || H / RD < 4 * n_sm)) RD /= 2;
+    while (RD > H) RD /= 2;
+    if (RD < rd_align || H % RD) return false;
+    if (RD * 2 * S > kStageBytes || RD * rowF > kStageBytes) return false;
+    if (S > 0 && RD * 2 * S + RD * rowF > kStageBytes) return false;  // sub-tile 0 holds shared + >= 1 expert
+    fp.RD = RD;
+    // region 0: x as given, w_sg and the logits (phase 1) -- later the int16 h cache
+    size_t o = up16((size_t)T * H * xsz);
+    fp.off_sig = (int)o;
+    o += up16((size_t)H * 2);
+    fp.off_lg = (int)o;
+    o += up16((size_t)T * E * 4);
+    fp.off_hq = 0;
+    o = std::max(o, up16((size_t)T * k * (F / 64) * kFragWords * 4));
+    fp.off_xq = (int)o;
+    o += up16((size_t)T * (H / 64) * kFragWords * 4);
+    fp.off_hsf = (int)o;
+    o += up16((size_t)T * S * 4);
+    fp.off_pbuf = (int)o;
+    o += (size_t)kCW * kMaxEnt * 4;
+    o = (o + 127) / 128 * 128;
+    fp.off_stages = (int)o;
+    const size_t fixed = (sizeof(FusedCtl) + 127) / 128 * 128 + o;
+    if (fixed + 2 * (size_t)kStageBytes > smem_max) return false;
+    fp.nstages = (int)std::min<size_t>(kMaxStages, (smem_max - fixed) / kStageBytes);
+    fp.smem = fixed + (size_t)fp.nstages * kStageBytes;
+    // a down task holds every sub-tile of its group at once: they must fit the ring with room to spare
+    const int bs = S > 0 ? RD * S * 2 : 0, be = RD * rowF;
+    const int m0 = (kStageBytes - bs) / be, mf = kStageBytes / be;
+    const int nsub_max = 1 + (na_max > m0 ? (na_max - m0 + mf - 1) / mf : 0);
+    if (nsub_max > fp.nstages - 1) return false;
+    return true;
+}
+
+// Per-device facts the launcher needs on every call, read once per device.
+struct DeviceFacts {
+    int n_sm = 0, smem_max = 0;
+    size_t smem_set[4] = {0, 0, 0, 0};  // dynamic smem limit set per kernel instantiation
+};
+constexpr int kMaxDevices = 64;
+static DeviceFacts g_dev[kMaxDevices];
+
+static cudaError_t device_facts(DeviceFacts** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    DeviceFacts& f = g_dev[dev];
+    if (f.n_sm == 0) {
+        int n = 0, m = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) return e;
+        f.smem_max = m;
+        f.n_sm = n;
+    }
+    *out = &f;
+    return cudaSuccess;
+}
+
+template <int MAXT, int SLOT>
+static cudaError_t launch_fused_t(const FusedParams& p, size_t smem, DeviceFacts& f, cudaStream_t st) {
+    const void* fn = (const void*)fused_decode_kernel<MAXT>;
+    if (f.smem_set[SLOT] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        f.smem_set[SLOT] = smem;
+    }
+    FusedParams pp = p;
+    void* args[] = {&pp};
+    // a cooperative launch fails (rather than deadlocks) if the grid cannot be co-resident
+    return cudaLaunchCooperativeKernel(fn, dim3(f.n_sm), dim3(kFusedThreads), args, smem, st);
+}
+
+bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err) {
+    DeviceFacts* f = nullptr;
+    *err = device_facts(&f);
+    if (*err != cudaSuccess) return false;
+    FusedPlanHost fp;
+    return plan_fused(s, T, f->n_sm, (size_t)f->smem_max, fp);
+}
+
+// Returns cudaErrorNotSupported when the shape is outside the fused kernel's plan.
+cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                                const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                                const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
+                                const WsLayout& W, cudaStream_t st) {
+    DeviceFacts* f = nullptr;
+    cudaError_t e = device_facts(&f);
+    if (e != cudaSuccess) return e;
+    FusedPlanHost fp;
+    if (!plan_fused(s, T, f->n_sm, (size_t)f->smem_max, fp)) return cudaErrorNotSupported;
+    FusedParams p;
+    p.x = x;
+    p.Wr = Wr;
+    p.bias = bias;
+    p.experts = experts;
+    p.stride = stride;
+    p.sg = sg;
+    p.su = su;
+    p.sd = sd;
+    p.ssig = ssig;
+    p.out = out;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    p.xlog = reinterpret_cast<uint64_t*>(base + W.xlog);
+    p.xhs = reinterpret_cast<uint64_t*>(base + W.xhs);
+    p.xh = reinterpret_cast<uint64_t*>(base + W.xh);
+    p.hdr = reinterpret_cast<WsHeader*>(base + W.header);
+    p.H = s.hidden;
+    p.E = s.n_experts;
+    p.k = s.top_k;
+    p.F = s.expert_ffn;
+    p.S = (sg != nullptr) ? s.shared_ffn : 0;
+    p.T = T;
+    p.x_dtype = s.x_dtype;
+    p.RR = fp.RR;
+    p.RS = fp.RS;
+    p.R = fp.R;
+    p.RD = fp.RD;
+    p.nstages = fp.nstages;
+    p.off_xq = fp.off_xq;
+    p.off_sig = fp.off_sig;
+    p.off_lg = fp.off_lg;
+    p.off_hsf = fp.off_hsf;
+    p.off_hq = fp.off_hq;
+    p.off_pbuf = fp.off_pbuf;
+    p.off_stages = fp.off_stages;
+    if (T == 1) return launch_fused_t<1, 0>(p, fp.smem, *f, st);
+    if (T <= 4) return launch_fused_t<4, 1>(p, fp.smem, *f, st);
+    if (T <= 8) return launch_fused_t<8, 2>(p, fp.smem, *f, st);
+    return launch_fused_t<16, 3>(p, fp.smem, *f, st);
+}
+
+}  // namespace qs

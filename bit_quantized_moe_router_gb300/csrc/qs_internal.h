@@ -1,0 +1,61 @@
+// qs_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qs_moe.h"
+
+namespace qs {
+
+// Workspace regions (byte offsets from the workspace base; each 256-aligned).
+struct WsLayout {
+    size_t header = 0;
+    size_t logits = 0;   // f32 [T x E]
+    size_t ids = 0;      // i32 [T x k]
+    size_t pw = 0;       // f32 [T x k]
+    size_t counts = 0;   // i32 [E]
+    size_t offsets = 0;  // i32 [E + 1]
+    size_t perm = 0;     // i32 [T x k]
+    size_t h = 0;        // f32 [T*k x F]
+    size_t hs = 0;       // f32 [T x S]
+    size_t gate = 0;     // f32 [T]
+    size_t tickets = 0;  // u32 [ceil(T / kRouteTok)]
+    // tagged exchanges of the persistent decode kernel: 64-bit (fp32 value | 32-bit call tag)
+    size_t xlog = 0;     // [Tf x E]
+    size_t xhs = 0;      // [Tf x S]
+    size_t xh = 0;       // [Tf*k x F]     (Tf = min(T, kFusedMaxT))
+    size_t total = 0;
+};
+
+constexpr int kRouteTok = 8;    // tokens per router CTA chunk
+constexpr int kFusedMaxT = 16;  // largest token count the persistent decode kernel takes
+
+WsLayout ws_layout(const qs_moe_shape& s, int max_tokens);
+
+// Decode-path launchers (qs_decode.cu).  All return the launch's cudaError_t.
+cudaError_t launch_route(const qs_moe_shape& s, const void* x, const float* W, const float* bias, int T,
+                         float* logits, int32_t* ids, float* pw, uint32_t* tickets, cudaStream_t st);
+cudaError_t launch_group(int E, int k, int T, const int32_t* ids, int32_t* counts, int32_t* offsets, int32_t* perm,
+                         cudaStream_t st);
+cudaError_t launch_gateup(const qs_moe_shape& s, const void* x, const uint8_t* experts, int64_t stride,
+                          const int32_t* offsets, const int32_t* perm, int T, float* h, cudaStream_t st);
+cudaError_t launch_down(const qs_moe_shape& s, const uint8_t* experts, int64_t stride, const float* h,
+                        const int32_t* ids, const float* pw, int n_slots, const uint16_t* sh_down,
+                        const float* hs, const float* gate, int T, float* out, int accumulate, cudaStream_t st);
+cudaError_t launch_shared_gateup(const qs_moe_shape& s, const void* x, const uint16_t* wg, const uint16_t* wu,
+                                 const uint16_t* wsig, int T, float* hs, float* gate, cudaStream_t st);
+cudaError_t launch_quantize(const float* w, int64_t n_blocks, uint8_t* out, cudaStream_t st);
+cudaError_t launch_test_wait(void* ws, uint64_t limit_ns, cudaStream_t st);
+
+// Persistent single-kernel decode path (qs_fused.cu).  cudaErrorNotSupported
+// when the shape or token count is outside its plan; the caller then runs the
+// per-step kernels.  sg == nullptr means no shared expert.
+cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                                const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                                const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
+                                const WsLayout& W, cudaStream_t st);
+bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err);
+
+}  // namespace qs
