@@ -22,6 +22,7 @@ EXPORTS = (
     "qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes", "qs_workspace_init",
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
     "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
+    "qs_moe_ffn_noalloc",
 )
 
 
@@ -81,6 +82,7 @@ def load(build_if_missing: bool = True):
     L.qs_shared_expert_ffn.argtypes = [SP, P, HP, i32, P, i32, P, sz, P]
     L.qs_moe_ffn.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
     L.qs_moe_ffn_launches.argtypes = [SP, i32, i32]
+    L.qs_moe_ffn_noalloc.argtypes = [SP, P, P, P, EP, HP, P, i32, P]
     L.qs_q2k_quantize.argtypes = [P, i64, i64, P, P]
     L.qs_test_wait_timeout.argtypes = [P, sz, i32, P]
     for name in EXPORTS:
@@ -187,6 +189,14 @@ def qs_moe_ffn(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared,
                              ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _ptr(out),
                              n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)), "qs_moe_ffn")
+
+
+def qs_moe_ffn_noalloc(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens,
+                       stream=None):
+    """The whole layer with its scratch in a fixed array inside the library (no workspace argument)."""
+    _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
+                                     ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
+                                     _ptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
 
 
 def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:

@@ -171,6 +171,25 @@ int qs_moe_ffn(const qs_moe_shape *shape, const void *x, const float *router_w, 
                const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                void *workspace, size_t workspace_bytes, void *stream);
 
+/* The whole layer without a workspace argument (the pages have no
+ * counterpart; this is a convenience of this library).  For callers that
+ * cannot allocate device memory -- an operator inside a framework that owns
+ * every device allocation and passes only inputs and outputs, or a serving loop
+ * under a fixed memory budget where cudaMalloc is not allowed once it runs.
+ * Same arguments and result as qs_moe_ffn minus the workspace; only the
+ * persistent decode kernel runs (n_tokens <= 16 and the shapes it plans for),
+ * otherwise QS_ERR_UNSUPPORTED.  Its scratch is a fixed 4 MiB array inside the
+ * library, held on every GPU that loads it until the process exits; a token
+ * count whose exchange area exceeds it returns QS_ERR_WORKSPACE.  The first
+ * call on a device looks the array up and zeroes it, synchronising `stream`,
+ * so make that first call before any stream capture.  Every call on a device
+ * shares the array and it keeps the last call's contents; calls that overlap
+ * on the GPU race on it.  Device-side time-outs are recorded in the array's
+ * status word, which this entry point does not report. */
+int qs_moe_ffn_noalloc(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
+                       const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
+                       void *stream);
+
 /* Number of kernels one qs_moe_ffn call with this shape, token count and
  * shared expert (has_shared != 0) launches on the current device: 1 for the
  * persistent decode kernel, more for the per-step path; 0 on an invalid
