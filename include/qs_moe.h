@@ -29,8 +29,9 @@
  *
  * Conventions of every entry point:
  *  - Pointers named device are device memory; the caller owns every buffer.
- *    The library allocates nothing and keeps no per-call state; it caches
- *    per-device facts (SM count, shared-memory limit) on first use.
+ *    The library allocates nothing (apart from the fixed array behind
+ *    qs_moe_ffn_noalloc) and keeps no per-call state; it caches per-device
+ *    facts (SM count, shared-memory limit) on first use.
  *  - All work is enqueued asynchronously on `stream` (a cudaStream_t; NULL =
  *    the legacy default stream).  Calls on one workspace must not overlap.
  *  - Host-detectable argument errors return QS_ERR_INVALID (or
