@@ -42,6 +42,13 @@ WsLayout ws_layout(const qs_moe_shape& s, int T) {
     L.xlog = take(tf * E * 8);
     L.xhs = take(tf * std::max<size_t>(S, 1) * 8);
     L.xh = take(tf * k * F * 8);
+    const size_t H = (size_t)s.hidden;
+    L.wr3 = take(3 * E * H * 2);
+    L.lpart = take((size_t)kPrefillMaxKS * t * E * 4);
+    L.xs = take(t * k * H * 2);
+    L.cursor = take(E * 4);
+    L.h16 = take(t * k * F * 2);
+    L.hs16 = take(t * std::max<size_t>(S, 1) * 2);
     L.total = o;
     return L;
 }
@@ -208,6 +215,13 @@ int qs_moe_ffn(const qs_moe_shape* shape, const void* x, const float* router_w, 
                                 st);
         if (e == cudaSuccess) return QS_OK;
         if (e != cudaErrorNotSupported) return cuda_fail(e);
+        e = launch_prefill(eff, x, router_w, router_bias, blocks, experts->expert_stride,
+                           has_shared ? (const uint16_t*)shared->w_gate : nullptr,
+                           has_shared ? (const uint16_t*)shared->w_up : nullptr,
+                           has_shared ? (const uint16_t*)shared->w_down : nullptr,
+                           has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, workspace, L, st);
+        if (e == cudaSuccess) return QS_OK;
+        if (e != cudaErrorNotSupported) return cuda_fail(e);
     }
     if (has_shared) {
         e = launch_shared_gateup(*shape, x, (const uint16_t*)shared->w_gate, (const uint16_t*)shared->w_up,
@@ -235,6 +249,7 @@ int qs_moe_ffn_launches(const qs_moe_shape* shape, int n_tokens, int has_shared)
     cudaError_t e;
     if (fused_decode_supported(eff, n_tokens, &e)) return 1;
     if (e != cudaSuccess) return -(int)e;
+    if (prefill_shape_ok(eff)) return prefill_launches();
     return eff.shared_ffn > 0 ? 5 : 4;
 }
 

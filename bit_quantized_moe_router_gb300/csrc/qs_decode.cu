@@ -87,6 +87,8 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(const void* __r
 // ====================================================================== (b) grouping
 
 // One CTA of 32*NW threads.  smem: hist[NW][E] + off[E+1] ints.
+constexpr int kGroupBatch = 8;  // id loads in flight per lane in group_kernel
+
 __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__ ids, int n, int E,
                                                      int32_t* counts, int32_t* offsets, int32_t* perm) {
     extern __shared__ int32_t gsm[];
@@ -98,9 +100,17 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
     __syncthreads();
     const int seg = (n + NW - 1) / NW;
     const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-    for (int i = s0 + lane; i < s1; i += 32) {
-        const int e = ids[i];
-        if ((unsigned)e < (unsigned)E) atomicAdd(&hist[warp * E + e], 1);
+    // ids are read in batches of kGroupBatch x 32 so that many loads are in flight at once
+    for (int base = s0; base < s1; base += 32 * kGroupBatch) {
+        int ev[kGroupBatch];
+#pragma unroll
+        for (int u = 0; u < kGroupBatch; u++) {
+            const int i = base + 32 * u + lane;
+            ev[u] = (i < s1) ? ids[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kGroupBatch; u++)
+            if ((unsigned)ev[u] < (unsigned)E) atomicAdd(&hist[warp * E + ev[u]], 1);
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -137,18 +147,27 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t* __restrict__
         }
     }
     __syncthreads();
-    for (int base = s0; base < s1; base += 32) {
-        const int i = base + lane;
-        const int e = (i < s1) ? ids[i] : -1;
-        const bool valid = (i < s1) && (unsigned)e < (unsigned)E;
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
-        if (valid) {
-            const int rank = __popc(peers & ((1u << lane) - 1u));
-            perm[off[e] + hist[warp * E + e] + rank] = i;
+    for (int base0 = s0; base0 < s1; base0 += 32 * kGroupBatch) {
+        int ev[kGroupBatch];
+#pragma unroll
+        for (int u = 0; u < kGroupBatch; u++) {
+            const int i = base0 + 32 * u + lane;
+            ev[u] = (i < s1) ? ids[i] : -1;
         }
-        __syncwarp();
-        if (valid && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
-        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < kGroupBatch; u++) {
+            const int i = base0 + 32 * u + lane;
+            const int e = ev[u];
+            const bool valid = (i < s1) && (unsigned)e < (unsigned)E;
+            const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : -1);
+            if (valid) {
+                const int rank = __popc(peers & ((1u << lane) - 1u));
+                perm[off[e] + hist[warp * E + e] + rank] = i;
+            }
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) hist[warp * E + e] += __popc(peers);
+            __syncwarp();
+        }
     }
 }
 

@@ -26,11 +26,19 @@ struct WsLayout {
     size_t xlog = 0;     // [Tf x E]
     size_t xhs = 0;      // [Tf x S]
     size_t xh = 0;       // [Tf*k x F]     (Tf = min(T, kFusedMaxT))
+    // tensor-core (prefill) path
+    size_t wr3 = 0;      // bf16 [3 x E x H]  router weights as three bf16 planes
+    size_t lpart = 0;    // f32 [kPrefillMaxKS x T x E] partial logits
+    size_t xs = 0;       // fp16 [T*k x H] token rows in expert-sorted order
+    size_t cursor = 0;   // i32 [E] fill pointers of the expert lists
+    size_t h16 = 0;      // fp16 [T*k x F] (expert-sorted entries)
+    size_t hs16 = 0;     // bf16 [T x S]
     size_t total = 0;
 };
 
 constexpr int kRouteTok = 8;    // tokens per router CTA chunk
 constexpr int kFusedMaxT = 16;  // largest token count the persistent decode kernel takes
+constexpr int kPrefillMaxKS = 4;  // largest split of H in the tensor-core router
 
 WsLayout ws_layout(const qs_moe_shape& s, int max_tokens);
 
@@ -57,5 +65,14 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
                                 const WsLayout& W, cudaStream_t st);
 bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err);
+
+// Tensor-core path for many tokens (qs_prefill.cu): prefill_launches() launches.  Needs bf16
+// x and Q2_K row layouts it can stage (see prefill_shape_ok).
+bool prefill_shape_ok(const qs_moe_shape& s);
+int prefill_launches();
+cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                           const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                           const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws, const WsLayout& W,
+                           cudaStream_t st);
 
 }  // namespace qs

@@ -164,10 +164,19 @@ int qs_shared_expert_ffn(const qs_moe_shape *shape, const void *x, const qs_shar
                          float *out, int accumulate, void *workspace, size_t workspace_bytes, void *stream);
 
 /* The whole layer: out [n_tokens x H] fp32 (overwritten) = routed experts
- * + gated shared expert (shared may be NULL or have S = 0).  Decode-sized
- * calls run one persistent kernel; large n_tokens run the grouped
- * tensor-core path.  workspace: qs_moe_workspace_bytes(shape, n_tokens)
- * bytes, initialised with qs_workspace_init. */
+ * + gated shared expert (shared may be NULL or have S = 0).  workspace:
+ * qs_moe_workspace_bytes(shape, n_tokens) bytes, initialised with
+ * qs_workspace_init.  Three implementations, picked per call:
+ *  - n_tokens <= 16 and a shape the persistent decode kernel plans for: one
+ *    kernel; the result does not depend on how tokens are batched;
+ *  - otherwise, with bf16 x (and Q2_K rows it can stage: hidden a multiple of
+ *    1024 or equal to 256; expert_ffn a multiple of 1024 or at most 768): the
+ *    tensor-core path -- router on the tensor cores as three exact bf16 planes
+ *    of router_w, experts as grouped GEMMs with Q2_K weights dequantised to
+ *    fp16 (the shared expert in bf16), fp32 accumulation, each routed
+ *    contribution p * (W_down h) rounded to fp16 and the k of a token summed in
+ *    slot order onto the shared expert's fp32 row;
+ *  - otherwise the per-step kernels (c)/(d) above. */
 int qs_moe_ffn(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
                const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                void *workspace, size_t workspace_bytes, void *stream);
@@ -193,8 +202,9 @@ int qs_moe_ffn_noalloc(const qs_moe_shape *shape, const void *x, const float *ro
 
 /* Number of kernels one qs_moe_ffn call with this shape, token count and
  * shared expert (has_shared != 0) launches on the current device: 1 for the
- * persistent decode kernel, more for the per-step path; 0 on an invalid
- * shape, negative (-cudaError_t) if the device query fails. */
+ * persistent decode kernel, 8 for the tensor-core path (which also issues a
+ * memset), 4 or 5 for the per-step path; 0 on an invalid shape, negative
+ * (-cudaError_t) if the device query fails. */
 int qs_moe_ffn_launches(const qs_moe_shape *shape, int n_tokens, int has_shared);
 
 /* Q2_K encoder (weight set-up, not part of the layer): round-to-nearest,
