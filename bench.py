@@ -197,6 +197,7 @@ def oracle_sample_layer(w, T, n_tokens, copy=0):
 def time_oracle(w, T, budget_s, max_calls=None):
     """Run the oracle, one layer call of T tokens at a time on one core, for ~budget_s seconds."""
     import oracle
+    T = min(T, ORACLE_TOKENS_MAX)
     n_pool = 16 if T == 1 else max(T, 16)
     xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
     calls, tokens = 0, 0
@@ -231,6 +232,8 @@ def run_reference(args, w, T):
         return
     import oracle
     oracle.build()
+    T_full = T
+    T = min(T, ORACLE_TOKENS_MAX)
     n_pool = max(T, 16)
     xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
 
@@ -247,17 +250,35 @@ def run_reference(args, w, T):
     ms = el / args.steps * 1e3
     val = T * args.steps / el
     line = {
-        "impl": "reference", "metric": "MoE-FFN layer tokens/s (batch %d decode)" % T, "value": val,
+        "impl": "reference", "metric": metric_name(T_full), "value": val,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": config_of(w, T, args),
+        "config": config_of(w, T_full, args),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} layer calls of {T} token(s) over a {n_pool}-token x pool, "
-                                   f"experts those tokens route to; {cpu_model()}"},
+                                   f"experts those tokens route to"
+                                   + (f" (the oracle's cost per token does not depend on the batch of {T_full})"
+                                      if T_full > T else "") + f"; {cpu_model()}"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+ORACLE_TOKENS_MAX = 16  # the oracle works token by token; large batches are timed on 16-token calls
+
+
+def metric_name(T):
+    return ("MoE-FFN layer tokens/s (batch %d decode)" % T) if T <= 16 else \
+        ("MoE-FFN layer tokens/s (prefill, %d tokens per call)" % T)
+
+
+def layer_flops(sh, T):
+    """Multiply-adds x2 the layer does per call: router, routed experts (3 matrices per slot), shared."""
+    router = 2 * T * sh.n_experts * sh.hidden
+    routed = 2 * T * sh.top_k * 3 * sh.expert_ffn * sh.hidden
+    shared = 2 * T * (3 * sh.shared_ffn * sh.hidden + sh.hidden)
+    return router + routed + shared
 
 
 def config_of(w, T, args):
@@ -344,8 +365,8 @@ def run_ours(args, w, T):
     layers = device_layers(w, qm, torch, device, copies)
 
     # x pool: rows wrap so that rows [j, j+T) are contiguous for every j < X_POOL
-    xb, _ = qi.gen_x(sh, w.seed, qi.X_POOL)
-    xwrap = np.concatenate([xb, xb[:T]], axis=0)
+    xb, _ = qi.gen_x(sh, w.seed, qi.X_POOL + (T if T > qi.X_POOL else 0))
+    xwrap = xb if T > qi.X_POOL else np.concatenate([xb, xb[:T]], axis=0)
     xdev = torch.from_numpy(xwrap.view(np.int16) if xwrap.dtype == np.uint16 else xwrap).to(device)
     ws = qm.alloc_workspace(shape, T)
     out = torch.empty((T, H), dtype=torch.float32, device=device)
@@ -453,27 +474,40 @@ def run_ours(args, w, T):
     cpu = None
     if not args.no_cpu_baseline and dist.world == 1:
         rate, calls, el = time_oracle(w, T, args.cpu_seconds)
+        ts = min(T, ORACLE_TOKENS_MAX)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{calls} layer calls of {T} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
-                         f"the experts they route to; {cpu_model()}"}
+               "sample": f"{calls} layer calls of {ts} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
+                         f"the experts they route to" + (" (per-token cost independent of the batch)" if T > ts else "")
+                         + f"; {cpu_model()}"}
+    if launches_per_step > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
+        flops = layer_flops(sh, T)
+        tf_peak = pk["bf16_tflops"] if pk else 1900.0
+        tf = flops / mean_step_s / 1e12
+        roof = {"bound": "tensor", "kernel": "qs_moe_ffn (whole layer, %d kernels)" % launches_per_step,
+                "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": tf / tf_peak,
+                "peak_source": ("MEASURED_PEAKS.json bf16_tflops, dense 16-bit burst (fp16 runs at the bf16 rate; "
+                                "of measured)") if pk else "fallback 1.9 PFLOP/s",
+                "algorithmic_flops_per_launch": flops, "traffic": None}
+    else:
+        roof = {"bound": "hbm",
+                "kernel": "fused_decode_kernel" if launches_per_step == 1 else "qs_moe_ffn (whole layer)",
+                "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
+                "algorithmic_bytes_per_launch": algo_bytes,
+                "traffic": recorded_traffic(w.name) if launches_per_step == 1 and T == w.tokens[0] else None}
     line = {
-        "metric": "MoE-FFN layer tokens/s (batch %d decode)" % T,
+        "metric": metric_name(T),
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step_s * 1e3, "us_per_layer": mean_step_s * 1e6,
         "us_per_layer_p10_p50_p90": [float(np.percentile(step_ms, q) * 1e3) for q in (10, 50, 90)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "q2k-int16dot-f32", "data": "synthetic",
+        "dtype": "q2k-int16dot-f32" if roof["bound"] == "hbm" else "q2k-dequant-f16-mma-f32", "data": "synthetic",
         "config": config_of(w, T, args),
         "achieved_gbs_all_bytes": achieved, "achieved_gbs_q2k_bytes": q2k_bytes / mean_step_s / 1e9,
-        "roofline": {"bound": "hbm",
-                     "kernel": "fused_decode_kernel" if launches_per_step == 1 else "qs_moe_ffn (whole layer)",
-                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
-                     "algorithmic_bytes_per_launch": algo_bytes,
-                     "traffic": recorded_traffic(w.name) if launches_per_step == 1 and T == w.tokens[0] else None},
+        "roofline": roof,
         "l2_flush": None if flush_ms is None else {
             "us_per_layer": flush_ms * 1e3, "frac": algo_bytes / (flush_ms / 1e3) / 1e9 / hbm_peak,
-            "note": "4 copies, L2 flushed between steps outside the events (kernel code evicted too)"},
+            "note": "%d layer copies, L2 flushed between steps outside the events (kernel code evicted too)" % w.copies},
         "e2e": {"value": tokens_total / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_stage.numel() * x_stage.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size())},

@@ -67,6 +67,7 @@ constexpr int kRouterStages = 3;
 constexpr int kRouterThreads = 192;
 constexpr int kMaxKS = kPrefillMaxKS;     // router split of H
 constexpr uint32_t kSleepNs = 20000;      // longest hardware suspension of a waiting thread per poll
+constexpr int kMaxCluster = 1;            // CTAs sharing B slices by multicast (1: no clusters)
 
 enum RawMode : int { kRawColumn = 0, kRawTile = 1 };
 
@@ -83,6 +84,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// The same box written to this CTA-relative offset in every CTA of `cta_mask`, each CTA's
+// mbarrier at `bar`'s offset receiving the completion.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
@@ -95,10 +106,24 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Record the first time-out: status = QS_ERR_TIMEOUT and, beside it in the workspace
+// header, which wait gave up (code), in which CTA, cluster rank and warp, at which counter.
+__device__ __noinline__ void note_timeout(uint32_t* status, uint32_t code, uint32_t counter) {
+    if (atomicCAS(status, 0u, (uint32_t)QS_ERR_TIMEOUT) == 0u) {
+        status[1] = code;
+        status[2] = blockIdx.x;
+        status[3] = cluster_ctarank();
+        status[4] = threadIdx.x >> 5;
+        status[5] = counter;
+        __threadfence();
+    }
+}
+
 // Bounded wait on an mbarrier phase by lane 0 of the warp, result broadcast to
 // the warp; on success every lane also observes the phase (acquire).  Returns
 // false at once if the CTA is aborting, or after the time limit (then aborts).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                          uint32_t code = 0, uint32_t counter = 0) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         if (!mbar_try_wait(bar, parity)) {
@@ -111,7 +136,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
                 }
                 if (global_timer_ns() - t0 > kWaitNs) {
                     *abort = 1;
-                    set_status(status, QS_ERR_TIMEOUT);
+                    note_timeout(status, code, counter);
                     ok = 0;
                     break;
                 }
@@ -123,7 +148,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return ok != 0;
 }
 // Bounded wait (lane 0 polls, result broadcast) until *tag == want.
-__device__ __forceinline__ bool warp_wait_tag(const int* tag, int want, volatile int* abort, uint32_t* status) {
+__device__ __forceinline__ bool warp_wait_tag(const int* tag, int want, volatile int* abort, uint32_t* status,
+                                              uint32_t code = 0) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) {
         const volatile int* t = tag;
@@ -136,7 +162,7 @@ __device__ __forceinline__ bool warp_wait_tag(const int* tag, int want, volatile
                 }
                 if (global_timer_ns() - t0 > kWaitNs) {
                     *abort = 1;
-                    set_status(status, QS_ERR_TIMEOUT);
+                    note_timeout(status, code, (uint32_t)want);
                     ok = 0;
                     break;
                 }
@@ -152,7 +178,8 @@ __device__ __forceinline__ bool warp_aborted(volatile int* abort) {
 }
 
 // The same for a single thread.
-__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status) {
+__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                            uint32_t code = 0, uint32_t counter = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
@@ -160,7 +187,7 @@ __device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity, vola
         if (*abort) return false;
         if (global_timer_ns() - t0 > kWaitNs) {
             *abort = 1;
-            set_status(status, QS_ERR_TIMEOUT);
+            note_timeout(status, code, counter);
             return false;
         }
     }
@@ -261,7 +288,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) pf_router_mma_kernel(const 
         if (lane == 0) {
             for (int i = 0; i < p.KBc; i++) {
                 const int s = i % kRouterStages;
-                if (i >= kRouterStages && !thread_wait(&ctl->empty[s], ((i / kRouterStages) - 1) & 1, abort, p.status))
+                if (i >= kRouterStages && !thread_wait(&ctl->empty[s], ((i / kRouterStages) - 1) & 1, abort, p.status, 12, i))
                     break;
                 uint8_t* st = sm + s * kStage;
                 mbar_arrive_expect_tx(&ctl->full[s], kStage);
@@ -276,7 +303,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) pf_router_mma_kernel(const 
             bool ok = true;
             for (int i = 0; i < p.KBc && ok; i++) {
                 const int s = i % kRouterStages;
-                ok = thread_wait(&ctl->full[s], (i / kRouterStages) & 1, abort, p.status);
+                ok = thread_wait(&ctl->full[s], (i / kRouterStages) & 1, abort, p.status, 13, i);
                 if (!ok) break;
                 tc::fence_after();
                 const uint32_t sa = smem_u32(sm + s * kStage);
@@ -293,7 +320,7 @@ __global__ void __launch_bounds__(kRouterThreads, 1) pf_router_mma_kernel(const 
         }
     } else {
         const int q = warp & 3;
-        const bool ok = warp_wait(&ctl->acc, 0, abort, p.status);
+        const bool ok = warp_wait(&ctl->acc, 0, abort, p.status, 14);
         tc::fence_after();
         if (ok) {
             const int e = m0 + 32 * q + lane;
@@ -475,7 +502,8 @@ struct ExpertParams {
     int K, Ks;           // routed / shared contraction length
     int MT, MTs;         // 128-row output tiles of the routed / shared matrices
     int E, k, T, F, S, H;
-    int n_shared_units;  // 0 when there is no shared expert
+    int n_sgroups;       // shared-expert token tiles (0 when there is no shared expert)
+    int cs;              // CTAs per cluster; they share each token tile's B slices by multicast
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
@@ -498,7 +526,7 @@ struct ExpertCtl {
     int raw_tag[kNRv];  // chunk number a raw slot is being filled with (set before the copy is issued)
     uint32_t tmem;
     int abort;
-    int n_units;
+    int n_groups;
     int pad;
     int col_row[4][kNT];    // epilogue warp q: per accumulator column, its token (shared) or entry (routed)
     float col_scale[4][kNT];  // ... and the routing weight / shared gate
@@ -520,32 +548,52 @@ struct Unit {
     int brow;    // first B row: token (shared) or sorted entry (routed)
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const ExpertParams& p, const ExpertTables& tb) {
+// Unit = (group g, output tile m).  Groups are token tiles: the shared expert's first, then each
+// expert's.  The CTAs of a cluster take the same groups; rank r takes tiles r, r + cs, ...
+__device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, const ExpertTables& tb) {
     Unit U;
-    if (u < p.n_shared_units) {
+    U.mt = m;
+    if (g < p.n_sgroups) {
         U.shared = 1;
         U.e = -1;
-        U.mt = u % p.MTs;
-        U.tok0 = (u / p.MTs) * kNT;
+        U.tok0 = g * kNT;
         U.n = min(kNT, p.T - U.tok0);
         U.brow = U.tok0;
         return U;
     }
-    u -= p.n_shared_units;
-    U.shared = 0;
-    U.mt = u % p.MT;
-    const int g = u / p.MT;
-    int lo = 0, hi = p.E;  // largest e with prefix[e] <= g
+    const int gg = g - p.n_sgroups;
+    int lo = 0, hi = p.E;  // largest e with prefix[e] <= gg
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (tb.prefix[mid] <= g) lo = mid;
+        if (tb.prefix[mid] <= gg) lo = mid;
         else hi = mid;
     }
+    U.shared = 0;
     U.e = lo;
-    U.tok0 = (g - tb.prefix[lo]) * kNT;
+    U.tok0 = (gg - tb.prefix[lo]) * kNT;
     U.n = min(kNT, tb.cnts[lo] - U.tok0);
     U.brow = tb.offs[lo] + U.tok0;
     return U;
+}
+
+// Iterate this CTA's units in order: body(U) for each; stop early when body returns false.
+template <class Body>
+__device__ __forceinline__ void for_units(const ExpertParams& p, const ExpertTables& tb, int n_groups, Body body) {
+    if (p.cs == 1) {  // no clusters: units (group-major) dealt to CTAs one by one, for balance
+        const int n_su = p.n_sgroups * p.MTs, n_units = n_su + (n_groups - p.n_sgroups) * p.MT;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const Unit U = (u < n_su) ? make_unit(u / p.MTs, u % p.MTs, p, tb)
+                                      : make_unit(p.n_sgroups + (u - n_su) / p.MT, (u - n_su) % p.MT, p, tb);
+            if (!body(U)) return;
+        }
+        return;
+    }
+    const int rank = (int)cluster_ctarank(), cid = (int)cluster_id_x(), ncl = (int)cluster_count_x();
+    for (int g = cid; g < n_groups; g += ncl) {
+        const int per = ((g < p.n_sgroups) ? p.MTs : p.MT) / p.cs;
+        for (int j = 0; j < per; j++)
+            if (!body(make_unit(g, rank + p.cs * j, p, tb))) return;
+    }
 }
 
 // Per-unit geometry shared by every role.
@@ -591,6 +639,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
     tb.cnts = tb.offs + p.E;
     volatile int* abort = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank();
+    // B stages are released to this CTA's own barrier and to the cluster leader's, which
+    // counts every CTA of the cluster before it multicasts the stage's next slice.
+    const uint16_t release_mask = (uint16_t)(1u | (1u << rank));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSA; s++) {
@@ -599,7 +651,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
         for (int s = 0; s < kNB; s++) {
             mbar_init(&ctl->bfull[s], 1);
-            mbar_init(&ctl->bempty[s], 1);
+            mbar_init(&ctl->bempty[s], rank == 0 ? p.cs : 1);
         }
         for (int r = 0; r < kNRv; r++) {
             mbar_init(&ctl->rawfull[r], 1);
@@ -623,7 +675,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         tb.offs[e] = p.offsets[e];
         tb.cnts[e] = p.counts[e];
     }
-    if (warp == 0) {  // unit tiles per expert: ceil(count / kNT), exclusive prefix
+    if (warp == 0) {  // token tiles per expert: ceil(count / kNT), exclusive prefix
         int carry = 0;
         for (int b = 0; b < p.E; b += 32) {
             const int e = b + lane;
@@ -639,14 +691,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
         if (lane == 0) {
             tb.prefix[p.E] = carry;
-            ctl->n_units = p.n_shared_units + carry * p.MT;
+            ctl->n_groups = p.n_sgroups + carry;
         }
     }
     tc::fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of every CTA initialised before any multicast reaches them
     tc::fence_after();
     const uint32_t tbase = ctl->tmem;
-    const int n_units = ctl->n_units;
+    const int n_groups = ctl->n_groups;
 
     if (warp < 8) {
         // ---------------------------------------------------------- dequant warps: raw slot -> TMEM A stage
@@ -663,12 +715,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 pend = -1;
             }
         };
-        for (int u = blockIdx.x; u < n_units && !warp_aborted(abort); u += gridDim.x) {
-            const Unit U = decode_unit(u, p, tb);
+        for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
+            if (warp_aborted(abort)) return false;
             const Geo g = unit_geo(U, p);
             if (U.shared) {  // the MMA reads shared-expert tiles straight from the raw slots
                 C += g.nch;
-                continue;
+                return true;
             }
             const int nblk = (p.raw_mode == kRawColumn) ? 1 : p.K / 256;  // Q2_K blocks per row per chunk
             bool ok = true;
@@ -677,8 +729,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 // Shared-expert chunks in between are consumed by the MMA, not by these warps, so
                 // they can be two fills ahead of the slot: wait for the slot to be tagged with this
                 // chunk before the phase-parity wait, which cannot tell phases two apart.
-                ok = warp_wait_tag(&ctl->raw_tag[slot], C, abort, p.status) &&
-                     warp_wait(&ctl->rawfull[slot], (C / kNRv) & 1, abort, p.status);
+                ok = warp_wait_tag(&ctl->raw_tag[slot], C, abort, p.status, 2) &&
+                     warp_wait(&ctl->rawfull[slot], (C / kNRv) & 1, abort, p.status, 1, C);
                 if (!ok) break;
                 const uint8_t* sl = raw + slot * kSlotBytes + m * kMatStride;
 #pragma unroll 1
@@ -721,7 +773,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         // dequantisation), wait for this slice's A stage, start this row's store
                         const int Gk = G + kb, s = Gk % NSA;
                         flush();
-                        if (Gk >= NSA && !warp_wait(&ctl->aempty[s], ((Gk / NSA) - 1) & 1, abort, p.status)) {
+                        if (Gk >= NSA && !warp_wait(&ctl->aempty[s], ((Gk / NSA) - 1) & 1, abort, p.status, 3, Gk)) {
                             ok = false;
                             break;
                         }
@@ -734,9 +786,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 if (lane == 0) mbar_arrive(&ctl->rawfree_d[slot]);
             }
             flush();  // before the next unit: the MMA must be able to finish this one
-            if (!ok) break;
             G += g.KB;
-        }
+            return ok;
+        });
         flush();
     } else if (warp < 12) {
         // ---------------------------------------------------------- epilogue warps
@@ -744,8 +796,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         int* crow = ctl->col_row[q];
         float* cscale = ctl->col_scale[q];
         int V = 0;
-        for (int u = blockIdx.x; u < n_units && !warp_aborted(abort); u += gridDim.x, V++) {
-            const Unit U = decode_unit(u, p, tb);
+        for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
+            if (warp_aborted(abort)) return false;
             const int b = V % NAB;
             if (NM == 1) {  // column metadata of this unit, read back as broadcasts below
                 for (int n = lane; n < U.n; n += 32) {
@@ -760,7 +812,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 }
                 __syncwarp();
             }
-            if (!warp_wait(&ctl->accfull[b], (V / NAB) & 1, abort, p.status)) break;
+            if (!warp_wait(&ctl->accfull[b], (V / NAB) & 1, abort, p.status, 4, V)) return false;
             tc::fence_after();
             const int o = U.mt * 128 + row;  // output feature (gate/up: f; down: h)
             if (NM == 2) {
@@ -802,32 +854,28 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             tc::fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->accempty[b]);
-        }
+            V++;
+            return true;
+        });
     } else if (warp == 12) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int GA = 0, GB = 0, C = 0, V = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x, V++) {
-                const Unit U = decode_unit(u, p, tb);
+            for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
+                if (*abort) return false;
                 const Geo g = unit_geo(U, p);
                 const int b = V % NAB;
-                if (V >= NAB) {
-                    ok = thread_wait(&ctl->accempty[b], ((V / NAB) - 1) & 1, abort, p.status);
-                    if (!ok) break;
-                }
+                if (V >= NAB && !thread_wait(&ctl->accempty[b], ((V / NAB) - 1) & 1, abort, p.status, 5, V)) return false;
                 tc::fence_after();
                 const int nmma = max(16, (U.n + 15) & ~15);
                 const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, 128, nmma);
                 for (int kb = 0; kb < g.KB; kb++) {
                     const int sb = (GB + kb) % kNB;
-                    ok = thread_wait(&ctl->bfull[sb], ((GB + kb) / kNB) & 1, abort, p.status);
-                    if (!ok) break;
+                    if (!thread_wait(&ctl->bfull[sb], ((GB + kb) / kNB) & 1, abort, p.status, 6, GB + kb)) return false;
                     const uint64_t bd = tc::sdesc_sw128(smem_u32(bst + sb * kBStageBytes));
                     if (U.shared) {
                         const int c = C + kb, slot = c % kNRv;
-                        ok = thread_wait(&ctl->rawfull[slot], (c / kNRv) & 1, abort, p.status);
-                        if (!ok) break;
+                        if (!thread_wait(&ctl->rawfull[slot], (c / kNRv) & 1, abort, p.status, 7, c)) return false;
                         tc::fence_after();
                         const uint32_t sa = smem_u32(raw + slot * kSlotBytes);
 #pragma unroll
@@ -841,8 +889,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         tc::commit(&ctl->rawfree_m[slot]);
                     } else {
                         const int Gk = GA + kb, s = Gk % NSA;
-                        ok = thread_wait(&ctl->afull[s], (Gk / NSA) & 1, abort, p.status);
-                        if (!ok) break;
+                        if (!thread_wait(&ctl->afull[s], (Gk / NSA) & 1, abort, p.status, 8, Gk)) return false;
                         tc::fence_after();
 #pragma unroll
                         for (int mq = 0; mq < NM; mq++) {
@@ -854,14 +901,16 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         }
                         tc::commit(&ctl->aempty[s]);
                     }
-                    tc::commit(&ctl->bempty[sb]);
+                    if (p.cs > 1) tc::commit_mc(&ctl->bempty[sb], release_mask);
+                    else tc::commit(&ctl->bempty[sb]);
                 }
-                if (!ok) break;
                 tc::commit(&ctl->accfull[b]);
                 GB += g.KB;
                 C += g.nch;
                 if (!U.shared) GA += g.KB;
-            }
+                V++;
+                return true;
+            });
             tc::commit(&ctl->drain);  // completes once every MMA issued above has
             (void)mbar_wait(&ctl->drain, 0);
         }
@@ -871,22 +920,23 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             int C = 0, GB = 0;
             int used_d[kNRv] = {}, used_m[kNRv] = {}, last[kNRv];  // last consumer of a slot: 0 none, 1 dequant, 2 MMA
             for (int i = 0; i < kNRv; i++) last[i] = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok && !*abort; u += gridDim.x) {
-                const Unit U = decode_unit(u, p, tb);
+            const uint16_t all_mask = (uint16_t)((1u << p.cs) - 1u);
+            for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
+                if (*abort) return false;
                 const Geo g = unit_geo(U, p);
                 const int row0 = U.mt * 128;
-                for (int kb = 0; kb < g.KB && ok; kb++) {
+                for (int kb = 0; kb < g.KB; kb++) {
                     if (kb % g.kpc == 0) {  // next raw chunk
                         const int ch = kb / g.kpc, slot = C % kNRv;
+                        bool ok = true;
                         if (last[slot] == 1) {
-                            ok = thread_wait(&ctl->rawfree_d[slot], used_d[slot] & 1, abort, p.status);
+                            ok = thread_wait(&ctl->rawfree_d[slot], used_d[slot] & 1, abort, p.status, 9, C);
                             used_d[slot]++;
                         } else if (last[slot] == 2) {
-                            ok = thread_wait(&ctl->rawfree_m[slot], used_m[slot] & 1, abort, p.status);
+                            ok = thread_wait(&ctl->rawfree_m[slot], used_m[slot] & 1, abort, p.status, 10, C);
                             used_m[slot]++;
                         }
-                        if (!ok) break;
+                        if (!ok) return false;
                         last[slot] = U.shared ? 2 : 1;
                         *reinterpret_cast<volatile int*>(&ctl->raw_tag[slot]) = C;
                         uint8_t* sl = raw + slot * kSlotBytes;
@@ -910,26 +960,34 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         }
                         C++;
                     }
+                    // B slice: the unit's rows only (one 128-row box, or 64 and/or 32-row boxes).
+                    // Each CTA expects the bytes on its own barrier once its previous use of the stage
+                    // is released; the cluster leader issues the copy, multicast to every CTA, once
+                    // every CTA has released the stage.
                     const int sb = GB % kNB;
-                    if (GB >= kNB) {
-                        ok = thread_wait(&ctl->bempty[sb], ((GB / kNB) - 1) & 1, abort, p.status);
-                        if (!ok) break;
-                    }
-                    // only the unit's rows: one 128-row box, or 64 and/or 32-row boxes
+                    if (GB >= kNB && !thread_wait(&ctl->bempty[sb], ((GB / kNB) - 1) & 1, abort, p.status, 11, GB))
+                        return false;
                     const CUtensorMap* mp = U.shared ? p.map_bs : p.map_br;
                     uint8_t* bs = bst + sb * kBStageBytes;
-                    if (U.n > 96) {
-                        mbar_arrive_expect_tx(&ctl->bfull[sb], kBStageBytes);
-                        tma_load_2d(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb]);
-                    } else {
-                        const int r64 = U.n > 32 ? 64 : 0, r32 = (U.n - r64 > 0) ? 32 : 0;
-                        mbar_arrive_expect_tx(&ctl->bfull[sb], (uint32_t)(r64 + r32) * 128u);
-                        if (r64) tma_load_2d(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb]);
-                        if (r32) tma_load_2d(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb]);
+                    const int r128 = U.n > 96 ? 128 : 0;
+                    const int r64 = (r128 == 0 && U.n > 32) ? 64 : 0;
+                    const int r32 = (r128 == 0 && U.n - r64 > 0) ? 32 : 0;
+                    mbar_arrive_expect_tx(&ctl->bfull[sb], (uint32_t)(r128 + r64 + r32) * 128u);
+                    if (rank == 0) {
+                        if (p.cs > 1) {
+                            if (r128) tma_load_2d_mc(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb], all_mask);
+                            if (r64) tma_load_2d_mc(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb], all_mask);
+                            if (r32) tma_load_2d_mc(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb], all_mask);
+                        } else {
+                            if (r128) tma_load_2d(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb]);
+                            if (r64) tma_load_2d(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb]);
+                            if (r32) tma_load_2d(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb]);
+                        }
                     }
                     GB++;
                 }
-            }
+                return true;
+            });
             if (*abort) {  // let issued copies land before the CTA exits
                 for (int i = 1; i <= kNRv && i <= C; i++) {
                     const int c = C - i;
@@ -949,6 +1007,16 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }
+    // No CTA leaves while a copy into its shared memory may still be in flight.  Without a
+    // time-out every CTA has consumed every slice sent to it.  After one, slices the leader
+    // issued may be unconsumed: once no CTA issues any more (first barrier), a CTA that gave
+    // up lets copies in flight land (they take microseconds) before anyone exits.
+    cluster_sync();
+    if (*abort && threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
+    }
+    cluster_sync();
 }
 
 // ================================================================== host side
@@ -1030,6 +1098,40 @@ size_t expert_smem(int E) {
     return 1024 + kNRv * kSlotBytes + kNB * kBStageBytes + sizeof(ExpertCtl<NM>) + 4 * (3 * E + 1);
 }
 size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCtl); }
+
+// Launch one expert kernel as clusters of p.cs CTAs (the largest of 8, 4, 2, 1 dividing the
+// routed and shared tile counts that the device can co-schedule), one CTA per SM.
+template <int NM>
+cudaError_t launch_expert(ExpertParams& p, int n_sm, int E, cudaStream_t st) {
+    const size_t smem = expert_smem<NM>(E);
+    for (int cs = kMaxCluster; cs >= 1; cs >>= 1) {
+        if (p.MT % cs || p.MTs % cs) continue;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kExpertThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((n_sm / cs) * cs);
+        int ncl = 0;
+        if (cs > 1) {
+            if (cudaOccupancyMaxActiveClusters(&ncl, pf_expert_kernel<NM>, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();
+                continue;
+            }
+            if (ncl < 1) continue;
+            cfg.gridDim = dim3(std::min(ncl, n_sm / cs) * cs);
+        }
+        p.cs = cs;
+        return cudaLaunchKernelEx(&cfg, pf_expert_kernel<NM>, p);
+    }
+    return cudaErrorNotSupported;
+}
 
 int router_splits(int E, int T, int H, int n_sm) {
     const int tiles = ((E + 127) / 128) * ((T + 127) / 128);
@@ -1135,7 +1237,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         if (S > 0) {
             p.Ks = (nm == 2) ? H : S;
             p.MTs = ((nm == 2) ? S : H) / 128;
-            p.n_shared_units = ((T + kNT - 1) / kNT) * p.MTs;
+            p.n_sgroups = (T + kNT - 1) / kNT;
             bool ok;
             if (nm == 2)
                 ok = encode_rows16(&p.map_s0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sg, H, S) &&
@@ -1147,8 +1249,8 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
             if (!ok) return cudaErrorInvalidValue;
         } else {
             p.Ks = 64;
-            p.MTs = 1;
-            p.n_shared_units = 0;
+            p.MTs = p.MT;
+            p.n_sgroups = 0;
         }
         p.counts = counts;
         p.offsets = offsets;
@@ -1190,10 +1292,8 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
     pf_scatter_kernel<<<(n + 7) / 8, 256, 0, st>>>(ids, n, k, H, static_cast<const uint16_t*>(x), cursor, perm, xs);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // (5) gate+up, (6) down
-    pf_expert_kernel<2><<<f->n_sm, kExpertThreads, expert_smem<2>(E), st>>>(ep[1]);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    pf_expert_kernel<1><<<f->n_sm, kExpertThreads, expert_smem<1>(E), st>>>(ep[0]);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_expert<2>(ep[1], f->n_sm, E, st)) != cudaSuccess) return e;
+    if ((e = launch_expert<1>(ep[0], f->n_sm, E, st)) != cudaSuccess) return e;
     // (7) y = shared + sum of the routed contributions
     const size_t groups = (size_t)T * H / 8;
     pf_combine_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, st>>>(xs, T, k, H, S > 0, out);

@@ -61,7 +61,9 @@ def run_layer(L, T, shared=True):
     out = torch.full((T, s.hidden), float("nan"), device="cuda")
     qm.qs_moe_ffn(shape, x, Wr, bias, ex, sh, out, T, ws)
     torch.cuda.synchronize()
-    assert qm.qs_read_device_status(ws) == qm.QS_OK
+    st = qm.qs_read_device_status(ws)
+    # on a device-side time-out the header also records which wait gave up, where
+    assert st == qm.QS_OK, f"status {st}, header {ws[:32].view(torch.int32).tolist()}"
     return out.cpu().numpy()
 
 
