@@ -27,7 +27,7 @@
 //   * a TMA thread streams the unit's raw weight bytes (Q2_K blocks or bf16
 //     rows) into a ring of shared-memory slots, and the unit's token rows
 //     (x, or h for the down projection) as 128B-swizzled B tiles into another;
-//   * eight dequant warps turn raw Q2_K bytes into fp16 weights and write
+//   * sixteen dequant warps turn raw Q2_K bytes into fp16 weights and write
 //     them straight into tensor memory, which is the MMA's A operand (the
 //     "TS" form: no shared-memory round trip for the dequantised weights);
 //     the shared expert's bf16 tiles are the A operand as they land (SS form);
@@ -62,12 +62,16 @@ constexpr int kMatStride = 16384;         // second matrix (up) inside a raw slo
 constexpr int kBStageBytes = kNT * 128;   // B operand stage: 128 rows x 64 16-bit values
 constexpr int kColBox = 112;              // bytes per row of a Q2_K column box (covers 84 + offset <= 12)
 constexpr int kA0 = 256;                  // first TMEM column of the A stages
-constexpr int kExpertThreads = 448;
+constexpr int kDeqWarps = 16;             // dequant warps of an expert kernel
+constexpr int kWarpMma = kDeqWarps + 4;   // MMA issuer (+ TMEM allocation)
+constexpr int kWarpRaw = kDeqWarps + 5;   // TMA of raw weights
+constexpr int kWarpB = kDeqWarps + 6;     // TMA of B slices
+constexpr int kExpertThreads = 32 * (kDeqWarps + 7);
 constexpr int kRouterStages = 3;
 constexpr int kRouterThreads = 192;
 constexpr int kMaxKS = kPrefillMaxKS;     // router split of H
 constexpr uint32_t kSleepNs = 20000;      // longest hardware suspension of a waiting thread per poll
-constexpr int kMaxCluster = 1;            // CTAs sharing B slices by multicast (1: no clusters)
+constexpr int kMaxCluster = 1;            // most CTAs sharing B slices by multicast (1: no clusters)
 
 enum RawMode : int { kRawColumn = 0, kRawTile = 1 };
 
@@ -101,6 +105,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
         "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
         : "memory");
 }
+// x < 2^23 as a float, exactly: x in the mantissa of 2^23, minus 2^23 (no int-to-float conversion).
+__device__ __forceinline__ float small_uint_to_float(uint32_t x) {
+    return __uint_as_float(0x4B000000u | x) - 8388608.0f;
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -196,31 +205,27 @@ __device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity, vola
 // ------------------------------------------------------------------ Q2_K -> fp16 for one 64-weight K slice
 
 // w[0..20]: the 84-byte block as words (scales 0..3, qs 4..19, d | dmin << 16 in 20).
-// K slice c (weights 64c .. 64c+63 of the block) -> 32 packed fp16 pairs, lower K in the low half.
-// Slice c uses scale bytes 4c..4c+3 (word c), code bytes 32(c>>1)..+31 (words 4+8(c>>1)..+7) and
-// bit pairs j = 2(c&1) and 2(c&1)+1; one code path serves every slice (the kernel stays small).
-__device__ __forceinline__ void dequant_slice(const uint32_t (&w)[21], int c, float d, float dm,
-                                              uint32_t (&out)[32]) {
-    const uint32_t scw = (c == 0) ? w[0] : (c == 1) ? w[1] : (c == 2) ? w[2] : w[3];
-    uint32_t qw[8];
+// K slice c (weights 64c .. 64c+63 of the block) uses scale bytes 4c..4c+3 (word c), code bytes
+// 32(c>>1)..+31 (words 4+8(c>>1)..+7) and bit pairs j = 2(c&1) + jj, jj = 0, 1.  Half jj of the
+// slice is weights 64c + 32jj .. +31 -> 16 packed fp16 pairs, lower K in the low half.  One code
+// path serves every slice (the kernel stays small); a half keeps register pressure low.
+__device__ __forceinline__ void dequant_half(uint32_t scw, const uint32_t (&qw)[8], int c, int jj, float d, float dm,
+                                             uint32_t (&out)[16]) {
+    const int sh = 4 * (c & 1) + 2 * jj;  // 2j
 #pragma unroll
-    for (int i = 0; i < 8; i++) qw[i] = (c >= 2) ? w[12 + i] : w[4 + i];
-    const int sh0 = 4 * (c & 1);  // 2j for the first bit pair
+    for (int lh = 0; lh < 2; lh++) {
+        const uint32_t sc = (scw >> (8 * (2 * jj + lh))) & 0xffu;
+        const float a = d * small_uint_to_float(sc & 15u), m = dm * small_uint_to_float(sc >> 4);
+        const uint32_t t0 = pack_h2(-m, a - m);
+        const uint32_t t1 = pack_h2(fmaf(2.0f, a, -m), fmaf(3.0f, a, -m));
 #pragma unroll
-    for (int jj = 0; jj < 2; jj++) {
-        const int sh = sh0 + 2 * jj;
-#pragma unroll
-        for (int lh = 0; lh < 2; lh++) {
-            const uint32_t sc = (scw >> (8 * (2 * jj + lh))) & 0xffu;
-            const float a = d * (float)(sc & 15u), m = dm * (float)(sc >> 4);
-            const uint32_t t0 = pack_h2(-m, a - m);
-            const uint32_t t1 = pack_h2(fmaf(2.0f, a, -m), fmaf(3.0f, a, -m));
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-                const uint32_t q = (qw[4 * lh + i] >> sh) & 0x03030303u;
-                out[16 * jj + 8 * lh + 2 * i] = __byte_perm(t0, t1, q * 34u + 0x1010u);
-                out[16 * jj + 8 * lh + 2 * i + 1] = __byte_perm(t0, t1, __umulhi(q, 34u << 16) + 0x1010u);
-            }
+        for (int i = 0; i < 4; i++) {
+            // bytes of q hold four weights' codes; byte b of sel selects table bytes (2q_b, 2q_b + 1):
+            // one selector for four weights, its upper half for the last two
+            const uint32_t q = (qw[4 * lh + i] >> sh) & 0x03030303u;
+            const uint32_t sel = q * 34u + 0x10101010u;
+            out[8 * lh + 2 * i] = __byte_perm(t0, t1, sel);
+            out[8 * lh + 2 * i + 1] = __byte_perm(t0, t1, sel >> 16);
         }
     }
 }
@@ -504,6 +509,7 @@ struct ExpertParams {
     int E, k, T, F, S, H;
     int n_sgroups;       // shared-expert token tiles (0 when there is no shared expert)
     int cs;              // CTAs per cluster; they share each token tile's B slices by multicast
+    int nt;              // token-tile height (MMA N limit)
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
@@ -556,8 +562,8 @@ __device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, c
     if (g < p.n_sgroups) {
         U.shared = 1;
         U.e = -1;
-        U.tok0 = g * kNT;
-        U.n = min(kNT, p.T - U.tok0);
+        U.tok0 = g * p.nt;
+        U.n = min(p.nt, p.T - U.tok0);
         U.brow = U.tok0;
         return U;
     }
@@ -570,8 +576,8 @@ __device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, c
     }
     U.shared = 0;
     U.e = lo;
-    U.tok0 = (gg - tb.prefix[lo]) * kNT;
-    U.n = min(kNT, tb.cnts[lo] - U.tok0);
+    U.tok0 = (gg - tb.prefix[lo]) * p.nt;
+    U.n = min(p.nt, tb.cnts[lo] - U.tok0);
     U.brow = tb.offs[lo] + U.tok0;
     return U;
 }
@@ -621,7 +627,8 @@ __device__ __forceinline__ Geo unit_geo(const Unit& U, const ExpertParams& p) {
 }
 
 // NM = 2: gate+up (two weight matrices share the B operand); NM = 1: down.
-// Warps 0..7 dequantise (routed units), 8..11 epilogue, 12 MMA (+TMEM), 13 TMA.
+// Warps 0..15 dequantise (routed units), 16..19 epilogue, 20 MMA (+TMEM), 21 TMA of raw weights,
+// 22 TMA of B slices.
 template <int NM>
 __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __grid_constant__ ExpertParams p) {
     using Ctl = ExpertCtl<NM>;
@@ -655,7 +662,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
         for (int r = 0; r < kNRv; r++) {
             mbar_init(&ctl->rawfull[r], 1);
-            mbar_init(&ctl->rawfree_d[r], 8);
+            mbar_init(&ctl->rawfree_d[r], kDeqWarps);
             mbar_init(&ctl->rawfree_m[r], 1);
         }
         for (int b = 0; b < 2; b++) {
@@ -667,7 +674,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         ctl->abort = 0;
         fence_barrier_init();
     }
-    if (warp == 12) {
+    if (warp == kWarpMma) {
         tc::tmem_alloc(&ctl->tmem, 512);
         tc::tmem_relinquish();
     }
@@ -675,11 +682,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         tb.offs[e] = p.offsets[e];
         tb.cnts[e] = p.counts[e];
     }
-    if (warp == 0) {  // token tiles per expert: ceil(count / kNT), exclusive prefix
+    if (warp == 0) {  // token tiles per expert: ceil(count / nt), exclusive prefix
         int carry = 0;
         for (int b = 0; b < p.E; b += 32) {
             const int e = b + lane;
-            const int c = (e < p.E) ? (p.counts[e] + kNT - 1) / kNT : 0;
+            const int c = (e < p.E) ? (p.counts[e] + p.nt - 1) / p.nt : 0;
             int s = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -700,10 +707,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
     const uint32_t tbase = ctl->tmem;
     const int n_groups = ctl->n_groups;
 
-    if (warp < 8) {
+    if (warp < kDeqWarps) {
         // ---------------------------------------------------------- dequant warps: raw slot -> TMEM A stage
-        const int grp = warp >> 2, q = warp & 3, r = 32 * q + lane;
-        const int m = (NM == 2) ? grp : 0;
+        // Warp w writes TMEM lane quarter q = w % 4 (rows 32q..32q+31) of matrix m (gate/up: bit 2
+        // of w) for the K slices kb with kb % n_slice_groups == its group.
+        const int q = warp & 3, r = 32 * q + lane;
+        const int m = (NM == 2) ? ((warp >> 2) & 1) : 0;
+        constexpr int kSliceGroups = (NM == 2) ? kDeqWarps / 8 : kDeqWarps / 4;
+        const int grp = (NM == 2) ? (warp >> 3) : (warp >> 2);
         int G = 0, C = 0;
         int pend = -1;  // A stage whose tensor-memory store was issued but not yet signalled
         auto flush = [&]() {
@@ -766,11 +777,15 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
 #pragma unroll 1
                     for (int c = 0; c < 4 && ok; c++) {
                         const int kb = kb0 + c;
-                        if (NM == 1 && (kb & 1) != grp) continue;
-                        uint32_t v[32];
-                        dequant_slice(w, c, d, dm, v);
-                        // signal the previous slice (its store has overlapped this slice's
-                        // dequantisation), wait for this slice's A stage, start this row's store
+                        if (kb % kSliceGroups != grp) continue;
+                        const uint32_t scw = (c == 0) ? w[0] : (c == 1) ? w[1] : (c == 2) ? w[2] : w[3];
+                        uint32_t qw[8];
+#pragma unroll
+                        for (int i = 0; i < 8; i++) qw[i] = (c >= 2) ? w[12 + i] : w[4 + i];
+                        uint32_t v[16];
+                        dequant_half(scw, qw, c, 0, d, dm, v);
+                        // signal the previous slice (its stores have overlapped this slice's
+                        // dequantisation), wait for this slice's A stage, store this row's 32 columns
                         const int Gk = G + kb, s = Gk % NSA;
                         flush();
                         if (Gk >= NSA && !warp_wait(&ctl->aempty[s], ((Gk / NSA) - 1) & 1, abort, p.status, 3, Gk)) {
@@ -778,7 +793,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                             break;
                         }
                         tc::fence_after();
-                        tc::st32(tc::taddr(tbase, 32 * q, kA0 + s * 32 * NM + m * 32), v);
+                        const uint32_t ta = tc::taddr(tbase, 32 * q, kA0 + s * 32 * NM + m * 32);
+                        tc::st16(ta, v);
+                        dequant_half(scw, qw, c, 1, d, dm, v);
+                        tc::st16(ta + 16, v);
                         pend = s;
                     }
                 }
@@ -790,7 +808,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             return ok;
         });
         flush();
-    } else if (warp < 12) {
+    } else if (warp < kWarpMma) {
         // ---------------------------------------------------------- epilogue warps
         const int q = warp & 3, row = 32 * q + lane;
         int* crow = ctl->col_row[q];
@@ -819,13 +837,13 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 uint16_t* dst = U.shared ? p.out_hs + (size_t)U.tok0 * p.S + o : p.out_h + (size_t)U.brow * p.F + o;
                 const size_t ld = U.shared ? (size_t)p.S : (size_t)p.F;
 #pragma unroll 1
-                for (int c0 = 0; c0 < U.n; c0 += 32) {  // warp-uniform
-                    uint32_t gv[32], uv[32];
-                    tc::ld32(tc::taddr(tbase, 32 * q, c0), gv);
-                    tc::ld32(tc::taddr(tbase, 32 * q, 128 + c0), uv);
+                for (int c0 = 0; c0 < U.n; c0 += 16) {  // warp-uniform
+                    uint32_t gv[16], uv[16];
+                    tc::ld16(tc::taddr(tbase, 32 * q, c0), gv);
+                    tc::ld16(tc::taddr(tbase, 32 * q, 128 + c0), uv);
                     tc::wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
+                    for (int i = 0; i < 16; i++) {
                         if (c0 + i < U.n) {
                             const float gq = __uint_as_float(gv[i]);
                             const float hv = __fdividef(gq, 1.0f + __expf(-gq)) * __uint_as_float(uv[i]);
@@ -857,7 +875,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             V++;
             return true;
         });
-    } else if (warp == 12) {
+    } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             int GA = 0, GB = 0, C = 0, V = 0;
@@ -915,29 +933,30 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             (void)mbar_wait(&ctl->drain, 0);
         }
     } else {
-        // ---------------------------------------------------------- TMA: raw weights and B tiles
+        // ---------------------------------------------------------- TMA: raw weights (warp 13), B slices (warp 14)
+        const bool do_raw = (warp == kWarpRaw), do_b = (warp == kWarpB);
         if (lane == 0) {
             int C = 0, GB = 0;
-            int used_d[kNRv] = {}, used_m[kNRv] = {}, last[kNRv];  // last consumer of a slot: 0 none, 1 dequant, 2 MMA
-            for (int i = 0; i < kNRv; i++) last[i] = 0;
+            int used_d[kNRv] = {}, used_m[kNRv] = {}, last_use[kNRv];  // last consumer: 0 none, 1 dequant, 2 MMA
+            for (int i = 0; i < kNRv; i++) last_use[i] = 0;
             const uint16_t all_mask = (uint16_t)((1u << p.cs) - 1u);
             for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
                 if (*abort) return false;
                 const Geo g = unit_geo(U, p);
                 const int row0 = U.mt * 128;
                 for (int kb = 0; kb < g.KB; kb++) {
-                    if (kb % g.kpc == 0) {  // next raw chunk
+                    if (do_raw && kb % g.kpc == 0) {  // next raw chunk
                         const int ch = kb / g.kpc, slot = C % kNRv;
                         bool ok = true;
-                        if (last[slot] == 1) {
+                        if (last_use[slot] == 1) {
                             ok = thread_wait(&ctl->rawfree_d[slot], used_d[slot] & 1, abort, p.status, 9, C);
                             used_d[slot]++;
-                        } else if (last[slot] == 2) {
+                        } else if (last_use[slot] == 2) {
                             ok = thread_wait(&ctl->rawfree_m[slot], used_m[slot] & 1, abort, p.status, 10, C);
                             used_m[slot]++;
                         }
                         if (!ok) return false;
-                        last[slot] = U.shared ? 2 : 1;
+                        last_use[slot] = U.shared ? 2 : 1;
                         *reinterpret_cast<volatile int*>(&ctl->raw_tag[slot]) = C;
                         uint8_t* sl = raw + slot * kSlotBytes;
                         uint64_t* bar = &ctl->rawfull[slot];
@@ -964,6 +983,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     // Each CTA expects the bytes on its own barrier once its previous use of the stage
                     // is released; the cluster leader issues the copy, multicast to every CTA, once
                     // every CTA has released the stage.
+                    if (!do_b) continue;
                     const int sb = GB % kNB;
                     if (GB >= kNB && !thread_wait(&ctl->bempty[sb], ((GB / kNB) - 1) & 1, abort, p.status, 11, GB))
                         return false;
@@ -989,13 +1009,22 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 return true;
             });
             if (*abort) {  // let issued copies land before the CTA exits
-                for (int i = 1; i <= kNRv && i <= C; i++) {
+                for (int i = 1; do_raw && i <= kNRv && i <= C; i++) {
                     const int c = C - i;
                     (void)mbar_wait(&ctl->rawfull[c % kNRv], (c / kNRv) & 1, 1000000ull);
                 }
-                for (int i = 1; i <= kNB && i <= GB; i++) {
+                for (int i = 1; do_b && i <= kNB && i <= GB; i++) {
                     const int c = GB - i;
                     (void)mbar_wait(&ctl->bfull[c % kNB], (c / kNB) & 1, 1000000ull);
+                }
+            }
+            // The peers' releases of the last B stages arrive here asynchronously (remote
+            // mbarrier arrivals): the leader must not leave while one is still on its way, or it
+            // lands in the shared memory of whatever runs next on this SM.
+            if (do_b && rank == 0 && p.cs > 1) {
+                for (int i = 1; i <= kNB && i <= GB; i++) {
+                    const int c = GB - i;
+                    (void)mbar_wait(&ctl->bempty[c % kNB], (c / kNB) & 1, *abort ? 1000000ull : kWaitNs);
                 }
             }
         }
@@ -1003,7 +1032,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
 
     tc::fence_before();
     __syncthreads();
-    if (warp == 12) {
+    if (warp == kWarpMma) {
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }
@@ -1228,6 +1257,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
             return cudaErrorInvalidValue;
         p.K = K;
         p.MT = ((nm == 2) ? F : H) / 128;
+        p.nt = kNT;
         p.E = E;
         p.k = k;
         p.T = T;
@@ -1237,7 +1267,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         if (S > 0) {
             p.Ks = (nm == 2) ? H : S;
             p.MTs = ((nm == 2) ? S : H) / 128;
-            p.n_sgroups = (T + kNT - 1) / kNT;
+            p.n_sgroups = (T + p.nt - 1) / p.nt;
             bool ok;
             if (nm == 2)
                 ok = encode_rows16(&p.map_s0, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, sg, H, S) &&
