@@ -124,6 +124,35 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
 __device__ __forceinline__ float tag_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
 __device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
 
+// This thread's share of a tagged exchange: words src[i0 + j * stride], j < n.  kPollBatch are
+// loaded at a time, so their latencies overlap; a word that does not carry this call's tag
+// yet is reloaded on its own until it does.  use(j, value) for each word.  False if the
+// CTA is aborting or the wait outlasts kWaitNs (measured from t0).
+constexpr int kPollBatch = 4;
+
+template <class Use>
+__device__ __forceinline__ bool poll_tagged(const uint64_t* src, int i0, int stride, int n, uint32_t tag,
+                                            const int* abort, uint64_t t0, Use use) {
+#pragma unroll 1
+    for (int b = 0; b < n; b += kPollBatch) {
+        uint64_t w[kPollBatch];
+#pragma unroll
+        for (int j = 0; j < kPollBatch; j++)
+            if (b + j < n) w[j] = ld_tagged(src + i0 + (size_t)(b + j) * stride);
+#pragma unroll
+        for (int j = 0; j < kPollBatch; j++) {
+            if (b + j < n) {
+                while (!tag_ok(w[j], tag)) {
+                    if (*reinterpret_cast<const volatile int*>(abort) || global_timer_ns() - t0 > kWaitNs) return false;
+                    w[j] = ld_tagged(src + i0 + (size_t)(b + j) * stride);
+                }
+                use(b + j, tag_value(w[j]));
+            }
+        }
+    }
+    return true;
+}
+
 // ------------------------------------------------------------------ tile and task bookkeeping
 
 struct Plan {
@@ -541,25 +570,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             // group-uniform outcome of the previous waits
             ok = group_count(2, !ok) == 0;
             if (ok) {
-                const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-                for (;;) {
-                    bool mine = true;
-#pragma unroll 1
-                    for (int i = gtid; i < T * E; i += kGT) {
-                        const uint64_t w = ld_tagged(P.xlog + i);
-                        mine &= tag_ok(w, tag);
-                        const float v = tag_value(w);
-                        lg[i] = (v == v) ? v : -INFINITY;  // a NaN logit ranks last
-                    }
-                    if (group_count(2, !mine) == 0) break;
-                    const bool late = gtid == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs);
-                    if (group_count(2, late) > 0) {
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(64);
-                }
+                // every thread polls only its own words, so a late word costs one reload of it
+                const int nw = gtid < T * E ? (T * E - gtid + kGT - 1) / kGT : 0;
+                const bool got = poll_tagged(P.xlog, gtid, kGT, nw, tag, &C.abort, global_timer_ns(),
+                                             [&](int j, float v) {
+                                                 lg[gtid + j * kGT] = (v == v) ? v : -INFINITY;  // NaN ranks last
+                                             });
+                ok = group_count(2, !got) == 0;
             }
             if (ok) {
                 // per 32-logit chunk: sort, keep the first k as candidates
@@ -586,7 +603,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     const float v = C.cand_v[q];
                     const int i = C.cand_i[q];
                     int rank = 0;
-#pragma unroll 1
+#pragma unroll 8
                     for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
                     if (rank < k && i < E) {
                         C.ids[t * k + rank] = i;
@@ -610,7 +627,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int i = gtid; i < n_ent; i += kGT) {
                     const int e = C.ids[i];
                     int rank = 0;
-#pragma unroll 1
+#pragma unroll 8
                     for (int j = 0; j < n_ent; j++) {
                         const int f = C.ids[j];
                         rank += (f < e) || (f == e && j < i);
@@ -638,7 +655,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                     const int t = C.ent_sorted[gtid] / k;
                     int pos = 0;
-#pragma unroll 1
+#pragma unroll 8
                     for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
                     C.tok_sorted[t * k + pos] = gtid;
                 }
@@ -823,23 +840,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 __threadfence_block();
                 const uint64_t t0 = global_timer_ns();
                 if (S > 0 && sidx == 0) {
-#pragma unroll 1
-                    for (;;) {
-                        bool mine = true;
-#pragma unroll 1
-                        for (int i = lane; i < T * S; i += 32) {
-                            const uint64_t w = ld_tagged(P.xhs + i);
-                            mine &= tag_ok(w, tag);
-                            hsf[i] = tag_value(w);
-                        }
-                        if (__all_sync(0xffffffffu, mine)) break;
-                        if (__any_sync(0xffffffffu, lane == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs))) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!ok) break;
+                    const int nw = (T * S - lane + 31) / 32;
+                    const bool got = poll_tagged(P.xhs, lane, 32, nw, tag, &C.abort, t0,
+                                                 [&](int j, float v) { hsf[lane + 32 * j] = v; });
+                    if (!(ok = __all_sync(0xffffffffu, got))) break;
                     __syncwarp();
                     if (lane == 0) {
                         __threadfence_block();
@@ -848,25 +852,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 } else {
                     const int ent = sidx - (S > 0 ? 1 : 0);
                     const uint64_t* hr = P.xh + (size_t)ent * F;
-                    float m;
-#pragma unroll 1
-                    for (;;) {
-                        bool mine = true;
-                        m = 0.0f;
-#pragma unroll 1
-                        for (int i = lane; i < F; i += 32) {
-                            const uint64_t w = ld_tagged(hr + i);
-                            mine &= tag_ok(w, tag);
-                            m = fmaxf(m, fabsf(tag_value(w)));
-                        }
-                        if (__all_sync(0xffffffffu, mine)) break;
-                        if (__any_sync(0xffffffffu, lane == 0 && (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs))) {
-                            ok = false;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                    if (!ok) break;
+                    float m = 0.0f;
+                    const bool got = poll_tagged(hr, lane, 32, (F - lane + 31) / 32, tag, &C.abort, t0,
+                                                 [&](int, float v) { m = fmaxf(m, fabsf(v)); });
+                    if (!(ok = __all_sync(0xffffffffu, got))) break;
                     m = warp_max(m);
                     const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
                     uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
