@@ -39,9 +39,9 @@ WsLayout ws_layout(const qs_moe_shape& s, int T) {
     L.gate = take(t * 4);
     L.tickets = take((t + kRouteTok - 1) / kRouteTok * 4);
     const size_t tf = std::min<size_t>(t, kFusedMaxT);
-    L.xlog = take(tf * E * 8);
-    L.xhs = take(tf * std::max<size_t>(S, 1) * 8);
-    L.xh = take(tf * k * F * 8);
+    L.xlog = take(tf * E * 4);
+    L.xhs = take(tf * std::max<size_t>(S, 1) * 4);
+    L.xh = take(tf * k * F * 4);
     const size_t H = (size_t)s.hidden;
     L.wr3 = take(3 * E * H * 2);
     L.lpart = take((size_t)kPrefillMaxKS * t * E * 4);

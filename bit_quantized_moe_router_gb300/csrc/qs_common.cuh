@@ -29,8 +29,9 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) <= kHeaderBytes, "header too large");
 
-// ctr[kCtrEpoch] holds the tag of the last completed persistent-decode call.
-enum Counter { kCtrExit = 2, kCtrTest = 3, kCtrEpoch = 5 };
+// Counters of the persistent decode kernel (tiles of logits, hs and h published; CTAs
+// that have left), zeroed by its last CTA out, and the counter of the wait test.
+enum Counter { kCtrLogits = 0, kCtrHs = 1, kCtrExit = 2, kCtrTest = 3, kCtrH = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -12,19 +12,25 @@
 //
 // Consumers work as independent warp tasks, so different warps can be in
 // different phases at once and nothing waits on a CTA-wide barrier:
-//   group A (warps 0-7):  router rows -> tagged logits; then the routing
+//   group A (warps 0-7):  router rows -> logits; then the routing
 //                         (top-k, softmax, grouping of the T*k entries by expert)
-//   group B (warps 8-15): x scales, int16 x and sigmoid gates; shared gate/up rows -> tagged hs
+//   group B (warps 8-15): x scales, int16 x and sigmoid gates; shared gate/up rows -> hs
 //   then every warp, round robin over the CTA's remaining tasks:
-//     routed gate/up rows -> tagged h;  staging of hs and of each entry's int16 h;
+//     routed gate/up rows -> h;  staging of hs and of each entry's int16 h;
 //     down rows: shared-expert down row + every active expert's down row -> out,
 //     summed in a fixed order (ascending expert id, then the gated shared expert)
 //
-// Cross-CTA exchange: logits, hs and h are written as 64-bit words (fp32
-// value | 32-bit call tag) and read by polling the words themselves.  The tag
-// of the last completed call lives in the workspace header; the last CTA to
-// leave advances it.  Every wait is bounded by the global timer; a wait that
-// runs out sets the sticky status QS_ERR_TIMEOUT and the CTA winds down.
+// Cross-CTA exchange: logits, hs and h are plain fp32 arrays in the workspace,
+// each with a completion counter in the workspace header.  A CTA that has
+// written its share of an array (all of its rows of that kind) adds the number
+// of tiles it wrote to the counter with one release reduction; one thread per
+// CTA waits with acquire loads until the counter reaches the array's tile
+// count, and only then does the CTA read the array, once.  (Readers that poll
+// the data words themselves keep the lines being written under a stream of
+// loads, and on this part that delays the writes by microseconds.)  The last
+// CTA to leave zeroes the counters for the next call.  Every wait is bounded
+// by the global timer; a wait that runs out sets the sticky status
+// QS_ERR_TIMEOUT and the CTA winds down.
 #include "qs_common.cuh"
 #include "qs_internal.h"
 #include "qs_q2k.cuh"
@@ -56,15 +62,15 @@ struct FusedParams {
     const uint16_t* sd;
     const uint16_t* ssig;
     float* out;
-    uint64_t* xlog;  // [T x E] tagged logits
-    uint64_t* xhs;   // [T x S] tagged hs
-    uint64_t* xh;    // [T*k x F] tagged h
+    float* xlog;  // [T x E] logits
+    float* xhs;   // [T x S] hs
+    float* xh;    // [T*k x F] h
     WsHeader* hdr;
     int H, E, k, F, S, T, x_dtype;
     int RR, RS, R, RD;  // rows per router, shared gate/up, routed gate/up and down tile
     int nstages;
     // byte offsets inside the data region that follows FusedCtl
-    int off_xq, off_sig, off_lg, off_hsf, off_hq, off_pbuf, off_stages;
+    int off_xq, off_sig, off_hsf, off_hq, off_pbuf, off_stages;
 };
 
 struct alignas(16) FusedCtl {
@@ -73,9 +79,10 @@ struct alignas(16) FusedCtl {
     uint64_t xbar;  // x and w_sg
     int done[kMaxStages];  // tasks finished on the tile now in each stage
     int slot_seq[kMaxStages];  // sequence number of the tile a stage is being filled with
-    int routed, xq_ready, hs_ready, abort, issued, n_active, shared_left, pad0;
-    uint32_t tag;  // this call's exchange tag
-    int pad[3];
+    int routed, xq_ready, hs_ready, abort, issued, n_active, shared_left, h_ready;
+    int et_left;   // routed gate/up tasks of this CTA not finished yet
+    int h_poller;  // set by the one warp that waits for the h counter
+    int pad[2];
     int ent_ready[kMaxEnt];
     int ids[kMaxEnt];
     float p[kMaxEnt];
@@ -112,43 +119,28 @@ __device__ __forceinline__ int group_count(int id, bool pred) {
 __device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 __device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
 
-__device__ __forceinline__ void st_tagged(uint64_t* p, float v, uint32_t tag) {
-    const uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+// Relaxed gpu-scope loads of exchanged data: served by L2, never by a stale L1 line.
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
 }
-__device__ __forceinline__ uint64_t ld_tagged(const uint64_t* p) {
-    uint64_t w;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
-    return w;
+__device__ __forceinline__ float4 ld_relaxed_f32x4(const float* p) {
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
 }
-__device__ __forceinline__ float tag_value(uint64_t w) { return __uint_as_float((uint32_t)w); }
-__device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
 
-// This thread's share of a tagged exchange: words src[i0 + j * stride], j < n.  kPollBatch are
-// loaded at a time, so their latencies overlap; a word that does not carry this call's tag
-// yet is reloaded on its own until it does.  use(j, value) for each word.  False if the
-// CTA is aborting or the wait outlasts kWaitNs (measured from t0).
-constexpr int kPollBatch = 4;
-
-template <class Use>
-__device__ __forceinline__ bool poll_tagged(const uint64_t* src, int i0, int stride, int n, uint32_t tag,
-                                            const int* abort, uint64_t t0, Use use) {
-#pragma unroll 1
-    for (int b = 0; b < n; b += kPollBatch) {
-        uint64_t w[kPollBatch];
-#pragma unroll
-        for (int j = 0; j < kPollBatch; j++)
-            if (b + j < n) w[j] = ld_tagged(src + i0 + (size_t)(b + j) * stride);
-#pragma unroll
-        for (int j = 0; j < kPollBatch; j++) {
-            if (b + j < n) {
-                while (!tag_ok(w[j], tag)) {
-                    if (*reinterpret_cast<const volatile int*>(abort) || global_timer_ns() - t0 > kWaitNs) return false;
-                    w[j] = ld_tagged(src + i0 + (size_t)(b + j) * stride);
-                }
-                use(b + j, tag_value(w[j]));
-            }
-        }
+// One thread: wait with acquire loads until the exchange counter *c reaches `target`.
+// False if the CTA is aborting or the wait outlasts kWaitNs.
+__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, const int* abort) {
+    if (ld_acquire(c) >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire(c) < target) {
+        if (*reinterpret_cast<const volatile int*>(abort) || global_timer_ns() - t0 > kWaitNs) return false;
     }
     return true;
 }
@@ -502,11 +494,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
     const bool x_f32 = P.x_dtype != QS_BF16;
     uint32_t* status = &P.hdr->status;
     uint32_t* ctr_exit = &P.hdr->ctr[kCtrExit][0];
-    uint32_t* epoch = &P.hdr->ctr[kCtrEpoch][0];
+    uint32_t* ctr_lg = &P.hdr->ctr[kCtrLogits][0];
+    uint32_t* ctr_hs = &P.hdr->ctr[kCtrHs][0];
+    uint32_t* ctr_h = &P.hdr->ctr[kCtrH][0];
     const uint8_t* xraw = data;                                              // [T x H] as given
     uint32_t* xqf = reinterpret_cast<uint32_t*>(data + P.off_xq);            // [T][H/64 chunks][36] fragments
     const uint8_t* sigbuf = data + P.off_sig;                                // [H] bf16
-    float* lg = reinterpret_cast<float*>(data + P.off_lg);                   // [T x E]
     float* hsf = reinterpret_cast<float*>(data + P.off_hsf);                 // [T x S]
     uint32_t* hqf = reinterpret_cast<uint32_t*>(data + P.off_hq);            // [T*k][F/64 chunks][36] fragments
     float* pbuf = reinterpret_cast<float*>(data + P.off_pbuf);               // [16 warps x kMaxEnt]
@@ -521,7 +514,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             C.slot_seq[i] = -1;
         }
         mbar_init(&C.xbar, 1);
-        C.routed = C.xq_ready = C.hs_ready = C.abort = C.issued = C.n_active = 0;
+        C.routed = C.xq_ready = C.hs_ready = C.h_ready = C.abort = C.issued = C.n_active = 0;
+        C.et_left = C.h_poller = 0;
         {
             const Plan L0 = make_plan(P);
             C.shared_left = L0.own_st * P.RS;  // shared gate/up row tasks of this CTA
@@ -536,14 +530,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         producer(P, C, data);
     } else {
         const Plan L = make_plan(P);
-        // this call's exchange tag: one past the epoch the previous call left (never 0)
-        uint32_t tag = 0;
-        if (lane == 0) {
-            tag = ld_acquire(epoch) + 1u;
-            if (tag == 0) tag = 1u;
-            if (warp == 0) C.tag = tag;
-        }
-        tag = __shfl_sync(0xffffffffu, tag, 0);
         const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
         bool ok = warp_wait_bar(C, &C.xbar, 0);
         if (!ok) fail(C, status);
@@ -562,20 +548,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const float b = P.bias ? P.bias[e] : 0.0f;
 #pragma unroll
                 for (int t = 0; t < MAXT; t++)
-                    if (t < T && lane == t) st_tagged(P.xlog + (size_t)t * E + e, acc[t] + b, tag);
+                    if (t < T && lane == t) P.xlog[(size_t)t * E + e] = acc[t] + b;
                 release_slot(C, m % ns, P.RR);
             }
             if (!ok) fail(C, status);
             // ------------------------------------------------------ group A: routing
-            // group-uniform outcome of the previous waits
+            // group-uniform outcome of the previous waits; the barrier also orders every
+            // logit this group stored before the release below
             ok = group_count(2, !ok) == 0;
             if (ok) {
-                // every thread polls only its own words, so a late word costs one reload of it
-                const int nw = gtid < T * E ? (T * E - gtid + kGT - 1) / kGT : 0;
-                const bool got = poll_tagged(P.xlog, gtid, kGT, nw, tag, &C.abort, global_timer_ns(),
-                                             [&](int j, float v) {
-                                                 lg[gtid + j * kGT] = (v == v) ? v : -INFINITY;  // NaN ranks last
-                                             });
+                bool got = true;
+                if (gtid == 0) {
+                    if (L.own_rt > 0) red_release_add(ctr_lg, (uint32_t)L.own_rt);
+                    got = wait_count(ctr_lg, (uint32_t)L.n_rt, &C.abort);
+                }
                 ok = group_count(2, !got) == 0;
             }
             if (ok) {
@@ -586,7 +572,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int q = gwarp; q < T * chunks; q += kGW) {
                     const int t = q / chunks, ch = q % chunks;
                     const int e = ch * 32 + lane;
-                    float v = e < E ? lg[t * E + e] : -INFINITY;
+                    float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
+                    if (v != v) v = -INFINITY;  // a NaN logit ranks last
                     int i = e < E ? e : 0x7fffffff;
                     warp_sort32(v, i);
                     if (lane < kc) {
@@ -661,6 +648,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 }
                 group_sync(2);
                 if (gtid == 0) {
+                    const int n_et = C.n_active * L.tpe;
+                    C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
                     __threadfence_block();
                     vstore(&C.routed, 1);
                 }
@@ -763,11 +752,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 warp_dense_row<MAXT>(st + (size_t)(P.RS + r) * H * 2, false, H, xraw, x_f32, T, ua);
 #pragma unroll
                 for (int t = 0; t < MAXT; t++)
-                    if (t < T && lane == t) st_tagged(P.xhs + (size_t)t * S + j * P.RS + r, silu(ga[t]) * ua[t], tag);
+                    if (t < T && lane == t) P.xhs[(size_t)t * S + j * P.RS + r] = silu(ga[t]) * ua[t];
                 release_slot(C, sq % ns, P.RS);
                 if (lane == 0) atomicSub(&C.shared_left, 1);
             }
             if (!ok) fail(C, status);
+            // every hs row of this CTA is stored: publish them (the barrier orders the stores)
+            if (group_count(3, !ok) == 0 && gtid == 0 && L.own_st > 0) red_release_add(ctr_hs, (uint32_t)L.own_st);
         }
 
         // ---------------------------------------------------------- every warp: the routed part
@@ -827,23 +818,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                     if (c0 == 0) {
                         const float sx = C.xscale[t] * (1.0f / 32767.0f);
-                        st_tagged(P.xh + (size_t)ent * F + tt * P.R + r, silu(gv * sx) * (uv * sx), tag);
+                        P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
                     }
                 }
-                release_slot(C, sq % ns, L.ept);
+                release_slot(C, sq % ns, L.ept);  // (its __syncwarp orders the lanes' h stores)
+                // the CTA's last routed task publishes all of the CTA's h tiles
+                if (lane == 0) {
+                    __threadfence_block();
+                    if (atomicSub(&C.et_left, 1) == 1) {
+                        __threadfence_block();
+                        red_release_add(ctr_h, (uint32_t)own_et);
+                    }
+                }
             } else if (q < q_et + n_stage_tasks) {
                 // ---------------------------------------------- staging of hs / of one entry's int16 h
                 const int sidx = q - q_et;
-                // the int16 h cache aliases x, w_sg and the logits: wait until their last reader is done
+                // the int16 h cache aliases x and w_sg: wait until their last reader is done
                 if (!(ok = warp_wait_flag(C, &C.xq_ready))) break;
                 if (!(ok = warp_wait_zero(C, &C.shared_left))) break;
                 __threadfence_block();
-                const uint64_t t0 = global_timer_ns();
                 if (S > 0 && sidx == 0) {
-                    const int nw = (T * S - lane + 31) / 32;
-                    const bool got = poll_tagged(P.xhs, lane, 32, nw, tag, &C.abort, t0,
-                                                 [&](int j, float v) { hsf[lane + 32 * j] = v; });
-                    if (!(ok = __all_sync(0xffffffffu, got))) break;
+                    int got = 1;
+                    if (lane == 0) got = wait_count(ctr_hs, (uint32_t)L.n_st, &C.abort);
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    __syncwarp();
+                    if (!(ok = got != 0)) break;
+#pragma unroll 4
+                    for (int i = lane * 4; i < T * S; i += 128)
+                        *reinterpret_cast<float4*>(hsf + i) = ld_relaxed_f32x4(P.xhs + i);
                     __syncwarp();
                     if (lane == 0) {
                         __threadfence_block();
@@ -851,22 +853,40 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                 } else {
                     const int ent = sidx - (S > 0 ? 1 : 0);
-                    const uint64_t* hr = P.xh + (size_t)ent * F;
+                    // the first entry task to get here waits for the h counter; the others for its flag
+                    int got = 1;
+                    if (lane == 0 && atomicCAS(&C.h_poller, 0, 1) == 0) {
+                        got = wait_count(ctr_h, (uint32_t)n_et, &C.abort);
+                        if (got) {
+                            __threadfence_block();
+                            vstore(&C.h_ready, 1);
+                        }
+                    }
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!(ok = got != 0 && warp_wait_flag(C, &C.h_ready))) break;
+                    __threadfence_block();
+                    const float* hr = P.xh + (size_t)ent * F;
+                    // lane: 8 consecutive values per 256; one pass for the scale, one to quantise
                     float m = 0.0f;
-                    const bool got = poll_tagged(hr, lane, 32, (F - lane + 31) / 32, tag, &C.abort, t0,
-                                                 [&](int, float v) { m = fmaxf(m, fabsf(v)); });
-                    if (!(ok = __all_sync(0xffffffffu, got))) break;
+#pragma unroll 2
+                    for (int p = lane * 8; p < F; p += 256) {
+                        const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
+                        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+                        m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+                    }
                     m = warp_max(m);
                     const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
                     uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
-#pragma unroll 1
+#pragma unroll 2
                     for (int p = lane * 8; p < F; p += 256) {
+                        const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
+                        const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
                         uint32_t wq[4];
                         int sum = 0;
 #pragma unroll
                         for (int q = 0; q < 4; q++) {
-                            const int a0 = __float2int_rn(tag_value(ld_tagged(hr + p + 2 * q)) * inv);
-                            const int a1 = __float2int_rn(tag_value(ld_tagged(hr + p + 2 * q + 1)) * inv);
+                            const int a0 = __float2int_rn(hv[2 * q] * inv);
+                            const int a1 = __float2int_rn(hv[2 * q + 1] * inv);
                             wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
                             sum += a0 + a1;
                         }
@@ -963,9 +983,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         if (vload(&C.abort)) set_status(status, QS_ERR_TIMEOUT);
         const uint32_t old = atom_acq_rel_add(ctr_exit, 1u);
         if (old == gridDim.x - 1) {
-            // last CTA out: every tagged word of this call has been read; advance the epoch
+            // last CTA out: every CTA is past its last counter wait; zero the counters for the next call
+            *reinterpret_cast<volatile uint32_t*>(ctr_lg) = 0u;
+            *reinterpret_cast<volatile uint32_t*>(ctr_hs) = 0u;
+            *reinterpret_cast<volatile uint32_t*>(ctr_h) = 0u;
             *reinterpret_cast<volatile uint32_t*>(ctr_exit) = 0u;
-            *reinterpret_cast<volatile uint32_t*>(epoch) = C.tag;
             __threadfence();
         }
     }
@@ -978,7 +1000,7 @@ static size_t up16(size_t v) { return (v + 15) / 16 * 16; }
 
 struct FusedPlanHost {
     int RR, RS, R, RD, nstages;
-    int off_xq, off_sig, off_lg, off_hsf, off_hq, off_pbuf, off_stages;
+    int off_xq, off_sig, off_hsf, off_hq, off_pbuf, off_stages;
     size_t smem;
 };
 
@@ -1010,12 +1032,10 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
     if (RD * 2 * S > kStageBytes || RD * rowF > kStageBytes) return false;
     if (S > 0 && RD * 2 * S + RD * rowF > kStageBytes) return false;  // sub-tile 0 holds shared + >= 1 expert
     fp.RD = RD;
-    // region 0: x as given, w_sg and the logits (phase 1) -- later the int16 h cache
+    // region 0: x as given and w_sg (phase 1) -- later the int16 h cache
     size_t o = up16((size_t)T * H * xsz);
     fp.off_sig = (int)o;
     o += up16((size_t)H * 2);
-    fp.off_lg = (int)o;
-    o += up16((size_t)T * E * 4);
     fp.off_hq = 0;
     o = std::max(o, up16((size_t)T * k * (F / 64) * kFragWords * 4));
     fp.off_xq = (int)o;
@@ -1108,9 +1128,9 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.ssig = ssig;
     p.out = out;
     uint8_t* base = static_cast<uint8_t*>(ws);
-    p.xlog = reinterpret_cast<uint64_t*>(base + W.xlog);
-    p.xhs = reinterpret_cast<uint64_t*>(base + W.xhs);
-    p.xh = reinterpret_cast<uint64_t*>(base + W.xh);
+    p.xlog = reinterpret_cast<float*>(base + W.xlog);
+    p.xhs = reinterpret_cast<float*>(base + W.xhs);
+    p.xh = reinterpret_cast<float*>(base + W.xh);
     p.hdr = reinterpret_cast<WsHeader*>(base + W.header);
     p.H = s.hidden;
     p.E = s.n_experts;
@@ -1126,7 +1146,6 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.nstages = fp.nstages;
     p.off_xq = fp.off_xq;
     p.off_sig = fp.off_sig;
-    p.off_lg = fp.off_lg;
     p.off_hsf = fp.off_hsf;
     p.off_hq = fp.off_hq;
     p.off_pbuf = fp.off_pbuf;

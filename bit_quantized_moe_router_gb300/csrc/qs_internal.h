@@ -22,7 +22,7 @@ struct WsLayout {
     size_t hs = 0;       // f32 [T x S]
     size_t gate = 0;     // f32 [T]
     size_t tickets = 0;  // u32 [ceil(T / kRouteTok)]
-    // tagged exchanges of the persistent decode kernel: 64-bit (fp32 value | 32-bit call tag)
+    // exchanged arrays of the persistent decode kernel (fp32; completion counters in the header)
     size_t xlog = 0;     // [Tf x E]
     size_t xhs = 0;      // [Tf x S]
     size_t xh = 0;       // [Tf*k x F]     (Tf = min(T, kFusedMaxT))
