@@ -13,14 +13,15 @@ Timing: W untimed warm-up steps, then K steps.  Inputs are resident in HBM.
 Default (--l2 cycle): inputs larger than L2 -- enough distinct layer copies are
 cycled that every weight byte a step reads was last touched more than three
 L2 capacities of traffic earlier, so it comes from HBM; steps run back to back
-(a sleep kernel queued first lets the host enqueue ahead of the GPU) and each
-step is bracketed by its own CUDA events.  --l2 flush: 4 copies, and between
-timed steps the L2 is flushed (512 MiB write + 256 MiB read) outside the
-step's events; this also evicts the kernel's own code, so it is the
-pessimistic figure; it is reported beside the default as `l2_flush`.  The step
-time is the sum of the per-step event intervals, max over ranks.  `e2e` times
-the same call through the public API with the step's x copied in from pinned
-host memory and y copied back, inside the events.
+(a sleep kernel queued first lets the host enqueue ahead of the GPU) and one
+pair of CUDA events brackets all K of them (an event recorded between two
+launches lengthens the gap between them, so per-step events would time
+themselves too).  --l2 flush: 4 copies, and between timed steps the L2 is
+flushed (512 MiB write + 256 MiB read) outside the step's own events; this
+also evicts the kernel's own code, so it is the pessimistic figure; it is
+reported beside the default as `l2_flush`.  Time is max over ranks.  `e2e`
+times the same K calls through the public API with each step's x copied in
+from pinned host memory and y copied back, all inside one event pair.
 
 Weights are drawn N(0, 0.02) on the device with torch's seeded generator
 (expert weights then quantised by the library's Q2_K encoder, shared weights
@@ -401,7 +402,10 @@ def run_ours(args, w, T):
         flush_r.sum()
 
     def timed(mode, n_layers, record_clocks):
-        """K steps; returns (per-step ms array, wall seconds, clocks)."""
+        """K steps; returns (ms of all K steps, wall seconds, clocks).  With inputs larger than L2
+        ("cycle") one event pair brackets the K back-to-back steps: an event recorded between two
+        launches lengthens the gap between them, so per-step pairs would time the events too.
+        With L2 flushes each step has its own pair, so that the flush kernels stay outside."""
         for i in range(args.warmup):
             if mode == "flush":
                 flush()
@@ -417,47 +421,52 @@ def run_ours(args, w, T):
         torch.cuda.nvtx.range_push("timed")
         if mode == "cycle":
             torch.cuda._sleep(int(2e6 + 120000 * K))  # let the host enqueue ahead of the GPU
-        for i in range(K):
-            if mode == "flush":
+        if mode == "flush":
+            for i in range(K):
                 flush()
-            evs[i][0].record(stream)
-            step(args.warmup + i, n_layers=n_layers)
-            evs[i][1].record(stream)
+                evs[i][0].record(stream)
+                step(args.warmup + i, n_layers=n_layers)
+                evs[i][1].record(stream)
+        else:
+            evs[0][0].record(stream)
+            for i in range(K):
+                step(args.warmup + i, n_layers=n_layers)
+            evs[0][1].record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
         dist.barrier()
         clk = clocks.stop() if clocks else None
-        return np.array([a.elapsed_time(b) for a, b in evs]), wall, clk
+        if mode == "flush":
+            return float(sum(a.elapsed_time(b) for a, b in evs)), wall, clk
+        return float(evs[0][0].elapsed_time(evs[0][1])), wall, clk
 
-    step_ms, wall, clk = timed(args.l2, None, True)
-    total_s = dist.max(float(step_ms.sum()) / 1e3)
+    total_ms, wall, clk = timed(args.l2, None, True)
+    total_s = dist.max(total_ms / 1e3)
     st = qm.qs_read_device_status(ws, stream)
     if st != qm.QS_OK:
         raise SystemExit(f"device status after the timed steps: {qm.status_string(st)}")
     flush_ms = None
     if args.l2 == "cycle":
         fl, _, _ = timed("flush", w.copies, False)
-        flush_ms = float(np.mean(fl))
+        flush_ms = fl / K
 
     # e2e through the public API: pinned host x in, y back out, inside the events
     x_host = torch.from_numpy(xwrap.view(np.int16) if xwrap.dtype == np.uint16 else xwrap).pin_memory()
     y_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
     x_stage = torch.empty_like(xdev[:T])
-    e2e_ev = []
     torch.cuda.synchronize()
     torch.cuda._sleep(int(2e6 + 160000 * K))
+    e2e_a, e2e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_a.record(stream)
     for i in range(K):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
         j = ((args.warmup + i) * T) % qi.X_POOL
         x_stage.copy_(x_host[j:j + T], non_blocking=True)
         step(args.warmup + i, x=x_stage)
         y_host.copy_(out, non_blocking=True)
-        b.record(stream)
-        e2e_ev.append((a, b))
+    e2e_b.record(stream)
     torch.cuda.synchronize()
-    e2e_s = dist.max(sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3)
+    e2e_s = dist.max(e2e_a.elapsed_time(e2e_b) / 1e3)
 
     # roofline of the layer kernel: algorithmic bytes over the measured step time
     algo = [algorithmic_bytes(sh, T, distinct[(args.warmup + j) % period]) for j in range(K)]
@@ -499,7 +508,6 @@ def run_ours(args, w, T):
         "metric": metric_name(T),
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step_s * 1e3, "us_per_layer": mean_step_s * 1e6,
-        "us_per_layer_p10_p50_p90": [float(np.percentile(step_ms, q) * 1e3) for q in (10, 50, 90)],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "q2k-int16dot-f32" if roof["bound"] == "hbm" else "q2k-dequant-f16-mma-f32", "data": "synthetic",
         "config": config_of(w, T, args),

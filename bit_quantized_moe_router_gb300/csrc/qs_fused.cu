@@ -1,6 +1,11 @@
 // qs_fused.cu -- the whole decode-sized MoE-FFN layer in one persistent kernel (sm_103a).
 //
-// One CTA per SM, launched cooperatively so every CTA is resident.  A CTA has
+// One CTA per SM (its shared memory admits no second one), every CTA resident at
+// once.  The kernel is a programmatic dependent launch: the next call in the
+// stream is launched while this one still runs, and its CTAs take each SM as
+// soon as this call's CTA there leaves.  Before it waits for the previous grid
+// (griddepcontrol.wait) the producer warp only prefetches weights into L2; no
+// thread touches x, the workspace or the output before that wait.  A CTA has
 // one producer warp and 16 consumer warps.  The producer streams the CTA's
 // tiles from HBM into a ring of 21 KB shared-memory stages with bulk
 // asynchronous copies (TMA engine): one "full" mbarrier per stage counts the
@@ -82,8 +87,8 @@ struct alignas(16) FusedCtl {
     int routed, xq_ready, hs_ready, abort, issued, n_active, shared_left, h_ready;
     int et_left;   // routed gate/up tasks of this CTA not finished yet
     int h_poller;  // set by the one warp that waits for the h counter
-    int pad[2];
-    int ent_ready[kMaxEnt];
+    int staged;    // entries whose int16 h is staged
+    int pad0;
     int ids[kMaxEnt];
     float p[kMaxEnt];
     float lsel[kMaxEnt];
@@ -270,6 +275,22 @@ __device__ __forceinline__ bool warp_wait_flag(FusedCtl& C, const int* flag) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// Whole warp waits until *v >= target (shared memory); false on abort or time-out.
+__device__ __forceinline__ bool warp_wait_geq(FusedCtl& C, const int* v, int target) {
+    bool ok = true;
+    if (vload(v) < target) {
+        const uint64_t t0 = global_timer_ns();
+        while (vload(v) < target) {
+            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void fail(FusedCtl& C, uint32_t* status) {
     if ((threadIdx.x & 31) == 0) {
         set_status(status, QS_ERR_TIMEOUT);
@@ -314,6 +335,27 @@ __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
     auto slot = [&](int s) { return stages + (size_t)(s % ns) * kStageBytes; };
     auto bar = [&](int s) { return &C.full[s % ns]; };
 
+    // weights first, into L2 only (the previous kernel in the stream may still be running and
+    // an L2 prefetch cannot make a later read stale), then wait for that kernel to complete
+#pragma unroll 1
+    for (int g = L.cta + lane * L.G; g < L.n_ind; g += 32 * L.G) {
+        if (g < L.n_rt) {
+            const uint32_t bytes = (uint32_t)P.RR * P.H * 4;
+            bulk_prefetch_l2(P.Wr + (size_t)g * P.RR * P.H, bytes);
+        } else {
+            const int j = g - L.n_rt;
+            const uint32_t bytes = (uint32_t)P.RS * P.H * 2;
+            bulk_prefetch_l2(P.sg + (size_t)j * P.RS * P.H, bytes);
+            bulk_prefetch_l2(P.su + (size_t)j * P.RS * P.H, bytes);
+        }
+    }
+    // the shared expert's down rows do not depend on the routing either: one slice per CTA
+    if (P.S > 0) {
+#pragma unroll 1
+        for (int r = L.cta + lane * L.G; r < P.H; r += 32 * L.G)
+            bulk_prefetch_l2(P.sd + (size_t)r * P.S, (uint32_t)P.S * 2);
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // x and the shared-expert gate vector first: group A and group B start on them
     {
         const uint32_t xb = (uint32_t)P.T * P.H * (P.x_dtype == QS_BF16 ? 2 : 4);
@@ -458,8 +500,9 @@ __device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int
         if (t < T) acc[t] = warp_sum(acc[t]);
 }
 
-// key order of the top-k: larger logit first, then the lower expert id
-__device__ __forceinline__ bool key_before(float v, int i, float ov, int oi) { return v > ov || (v == ov && i < oi); }
+// key order of the top-k: larger logit first, then the lower expert id.  Evaluated without
+// short-circuit so that it compiles to predicate logic, not to branches.
+__device__ __forceinline__ bool key_before(float v, int i, float ov, int oi) { return (v > ov) | ((v == ov) & (i < oi)); }
 
 // Sort 32 (value, index) pairs held one per lane into key order (bitonic network).
 __device__ __forceinline__ void warp_sort32(float& v, int& i) {
@@ -472,11 +515,75 @@ __device__ __forceinline__ void warp_sort32(float& v, int& i) {
             const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
             const bool first = (lane & size) == 0 || size == 32;  // this block ends up in key order
             const bool lower = (lane & stride) == 0;
-            const bool mine_first = key_before(v, i, ov, oi);
-            if ((lower == first) ? !mine_first : mine_first) {
-                v = ov;
-                i = oi;
+            const bool take = (lower == first) != key_before(v, i, ov, oi);
+            v = take ? ov : v;
+            i = take ? oi : i;
+        }
+    }
+}
+
+// Compare-exchange of two (value, index) pairs so that slot a holds the one first in key order.
+// Selects, not a conditional swap: a data-dependent branch here diverges the warp and costs
+// several times the arithmetic.
+__device__ __forceinline__ void key_cx(float& va, int& ia, float& vb, int& ib) {
+    const bool sw = key_before(vb, ib, va, ia);
+    const float a = sw ? vb : va, b = sw ? va : vb;
+    const int x = sw ? ib : ia, y = sw ? ia : ib;
+    va = a;
+    vb = b;
+    ia = x;
+    ib = y;
+}
+
+// Sorts the 8 pairs a lane holds into key order (bitonic network, registers only).
+__device__ __forceinline__ void sort8(float (&v)[8], int (&id)[8]) {
+#pragma unroll
+    for (int size = 2; size <= 8; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int m = 0; m < 8; m++) {
+                const int o = m ^ stride;
+                if (o > m) {
+                    if ((m & size) == 0 || size == 8) key_cx(v[m], id[m], v[o], id[o]);
+                    else key_cx(v[o], id[o], v[m], id[m]);
+                }
             }
+        }
+    }
+}
+
+// One warp: the 8 first entries in key order (larger logit first, then the lower expert id)
+// of E <= 256 logits at `lg`, lane l holding logits l, l + 32, ...  Each lane sorts its 8,
+// then five butterfly steps merge the lane's list with its partner's (the first 8 of two
+// sorted lists: pairwise the better of a[m] and b[7 - m], then a bitonic clean-up), so
+// every lane ends with the same sorted top-8.  A NaN logit ranks below every number.
+__device__ __forceinline__ void warp_top8(const float* lg, int E, float (&v)[8], int (&id)[8]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+        const int e = lane + 32 * m;
+        float x = e < E ? ld_relaxed_f32(lg + e) : -INFINITY;
+        v[m] = (x == x) ? x : -INFINITY;
+        id[m] = e < E ? e : 0x7fffffff;
+    }
+    sort8(v, id);
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        float ov[8];
+        int oi[8];
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+            ov[m] = __shfl_xor_sync(0xffffffffu, v[7 - m], d);
+            oi[m] = __shfl_xor_sync(0xffffffffu, id[7 - m], d);
+        }
+#pragma unroll
+        for (int m = 0; m < 8; m++) key_cx(v[m], id[m], ov[m], oi[m]);
+#pragma unroll
+        for (int stride = 4; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int m = 0; m < 8; m++)
+                if ((m & stride) == 0) key_cx(v[m], id[m], v[m + stride], id[m + stride]);
         }
     }
 }
@@ -515,20 +622,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         }
         mbar_init(&C.xbar, 1);
         C.routed = C.xq_ready = C.hs_ready = C.h_ready = C.abort = C.issued = C.n_active = 0;
-        C.et_left = C.h_poller = 0;
+        C.et_left = C.h_poller = C.staged = 0;
         {
             const Plan L0 = make_plan(P);
             C.shared_left = L0.own_st * P.RS;  // shared gate/up row tasks of this CTA
         }
         fence_barrier_init();
     }
-#pragma unroll 1
-    for (int i = tid; i < kMaxEnt; i += blockDim.x) C.ent_ready[i] = 0;
     __syncthreads();
+    if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == kCW) {
         producer(P, C, data);
     } else {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const Plan L = make_plan(P);
         const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
         bool ok = warp_wait_bar(C, &C.xbar, 0);
@@ -565,93 +672,143 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 ok = group_count(2, !got) == 0;
             }
             if (ok) {
-                // per 32-logit chunk: sort, keep the first k as candidates
-                const int chunks = (E + 31) / 32;
-                const int kc = min(k, 32);
+                // small routers (E <= 256, k <= 8): one warp per token, top-k and softmax in registers
+                const bool fast = E <= 256 && k <= 8;
+                if (fast) {
 #pragma unroll 1
-                for (int q = gwarp; q < T * chunks; q += kGW) {
-                    const int t = q / chunks, ch = q % chunks;
-                    const int e = ch * 32 + lane;
-                    float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
-                    if (v != v) v = -INFINITY;  // a NaN logit ranks last
-                    int i = e < E ? e : 0x7fffffff;
-                    warp_sort32(v, i);
-                    if (lane < kc) {
-                        C.cand_v[q * kc + lane] = v;
-                        C.cand_i[q * kc + lane] = i;
+                    for (int t = gwarp; t < T; t += kGW) {
+                        float v[8];
+                        int id[8];
+                        warp_top8(P.xlog + (size_t)t * E, E, v, id);
+                        float den = 0.0f;
+#pragma unroll
+                        for (int m = 0; m < 8; m++)
+                            if (m < k) den += expf(v[m] - v[0]);
+#pragma unroll
+                        for (int m = 0; m < 8; m++) {
+                            if (m < k && lane == m) {
+                                C.ids[t * k + m] = id[m];
+                                C.p[t * k + m] = expf(v[m] - v[0]) / den;
+                                if (T == 1) {
+                                    // one token's k ids are distinct: the rank by id is the grouping
+                                    int rank = 0;
+#pragma unroll
+                                    for (int i = 0; i < 8; i++)
+                                        if (i < k) rank += id[i] < id[m];
+                                    C.ent_sorted[rank] = m;
+                                    C.es[rank] = id[m];
+                                    C.act_e[rank] = id[m];
+                                    C.act_begin[rank] = rank;
+                                    C.tok_sorted[rank] = rank;
+                                }
+                            }
+                        }
+                        if (T == 1 && lane == 0) {
+                            C.act_begin[k] = k;
+                            C.n_active = k;
+                        }
                     }
-                }
-                group_sync(2);
-                // rank among the token's candidates: rank < k is selected
-                const int nc = chunks * kc;
+                } else {
+                    // per 32-logit chunk: sort, keep the first k as candidates
+                    const int chunks = (E + 31) / 32;
+                    const int kc = min(k, 32);
 #pragma unroll 1
-                for (int q = gtid; q < T * nc; q += kGT) {
-                    const int t = q / nc;
-                    const float v = C.cand_v[q];
-                    const int i = C.cand_i[q];
-                    int rank = 0;
+                    for (int q = gwarp; q < T * chunks; q += kGW) {
+                        const int t = q / chunks, ch = q % chunks;
+                        const int e = ch * 32 + lane;
+                        float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
+                        if (v != v) v = -INFINITY;  // a NaN logit ranks last
+                        int i = e < E ? e : 0x7fffffff;
+                        warp_sort32(v, i);
+                        if (lane < kc) {
+                            C.cand_v[q * kc + lane] = v;
+                            C.cand_i[q * kc + lane] = i;
+                        }
+                    }
+                    group_sync(2);
+                    // rank among the token's candidates: rank < k is selected
+                    const int nc = chunks * kc;
+#pragma unroll 1
+                    for (int q = gtid; q < T * nc; q += kGT) {
+                        const int t = q / nc;
+                        const float v = C.cand_v[q];
+                        const int i = C.cand_i[q];
+                        int rank = 0;
 #pragma unroll 8
-                    for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
-                    if (rank < k && i < E) {
-                        C.ids[t * k + rank] = i;
-                        C.lsel[t * k + rank] = v;
+                        for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
+                        if (rank < k && i < E) {
+                            C.ids[t * k + rank] = i;
+                            C.lsel[t * k + rank] = v;
+                        }
+                    }
+                    group_sync(2);
+                    // softmax over the selected logits (one warp per token)
+#pragma unroll 1
+                    for (int t = gwarp; t < T; t += kGW) {
+                        const float l0 = C.lsel[t * k];
+                        float ex = 0.0f;
+#pragma unroll 1
+                        for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
+                        const float den = warp_sum(ex);
+#pragma unroll 1
+                        for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
                     }
                 }
-                group_sync(2);
-                // softmax over the selected logits (one warp per token)
+                if (fast && T == 1) {
+                    if (gwarp == 0) {
+                        __syncwarp();
+                        if (lane == 0) {
+                            C.et_left = owned_count(L.n_ind, L.n_ind + k * L.tpe, L.G, L.cta) * L.ept;
+                            __threadfence_block();
+                            vstore(&C.routed, 1);
+                        }
+                    }
+                } else {
+                    if (fast) group_sync(2);
+                    // order the entries by (expert, entry)
 #pragma unroll 1
-                for (int t = gwarp; t < T; t += kGW) {
-                    const float l0 = C.lsel[t * k];
-                    float ex = 0.0f;
-#pragma unroll 1
-                    for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
-                    const float den = warp_sum(ex);
-#pragma unroll 1
-                    for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
-                }
-                // order the entries by (expert, entry)
-#pragma unroll 1
-                for (int i = gtid; i < n_ent; i += kGT) {
-                    const int e = C.ids[i];
-                    int rank = 0;
+                    for (int i = gtid; i < n_ent; i += kGT) {
+                        const int e = C.ids[i];
+                        int rank = 0;
 #pragma unroll 8
-                    for (int j = 0; j < n_ent; j++) {
-                        const int f = C.ids[j];
-                        rank += (f < e) || (f == e && j < i);
+                        for (int j = 0; j < n_ent; j++) {
+                            const int f = C.ids[j];
+                            rank += (f < e) || (f == e && j < i);
+                        }
+                        C.ent_sorted[rank] = i;
+                        C.es[rank] = e;
                     }
-                    C.ent_sorted[rank] = i;
-                    C.es[rank] = e;
-                }
-                group_sync(2);
-                // active experts: a run start in es[] opens a new active expert
-                const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
-                const unsigned bal = __ballot_sync(0xffffffffu, start);
-                if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
-                group_sync(2);
-                if (gtid < n_ent) {
-                    int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+                    group_sync(2);
+                    // active experts: a run start in es[] opens a new active expert
+                    const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
+                    const unsigned bal = __ballot_sync(0xffffffffu, start);
+                    if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
+                    group_sync(2);
+                    if (gtid < n_ent) {
+                        int a = __popc(bal & ((2u << lane) - 1u)) - 1;
 #pragma unroll 1
-                    for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
-                    if (start) {
-                        C.act_e[a] = C.es[gtid];
-                        C.act_begin[a] = gtid;
-                    }
-                    if (gtid == n_ent - 1) {
-                        C.act_begin[a + 1] = n_ent;
-                        C.n_active = a + 1;
-                    }
-                    const int t = C.ent_sorted[gtid] / k;
-                    int pos = 0;
+                        for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
+                        if (start) {
+                            C.act_e[a] = C.es[gtid];
+                            C.act_begin[a] = gtid;
+                        }
+                        if (gtid == n_ent - 1) {
+                            C.act_begin[a + 1] = n_ent;
+                            C.n_active = a + 1;
+                        }
+                        const int t = C.ent_sorted[gtid] / k;
+                        int pos = 0;
 #pragma unroll 8
-                    for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
-                    C.tok_sorted[t * k + pos] = gtid;
-                }
-                group_sync(2);
-                if (gtid == 0) {
-                    const int n_et = C.n_active * L.tpe;
-                    C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
-                    __threadfence_block();
-                    vstore(&C.routed, 1);
+                        for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
+                        C.tok_sorted[t * k + pos] = gtid;
+                    }
+                    group_sync(2);
+                    if (gtid == 0) {
+                        const int n_et = C.n_active * L.tpe;
+                        C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
+                        __threadfence_block();
+                        vstore(&C.routed, 1);
+                    }
                 }
             } else {
                 fail(C, status);
@@ -900,7 +1057,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     __syncwarp();
                     if (lane == 0) {
                         __threadfence_block();
-                        vstore(&C.ent_ready[ent], 1);
+                        atomicAdd(&C.staged, 1);
                     }
                 }
             } else {
@@ -913,56 +1070,101 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 1
                 for (int s = 0; ok && s < nsub; s++) ok = warp_wait_tile(C, sq0 + s, ns);
                 if (ok && S > 0) ok = warp_wait_flag(C, &C.hs_ready);
-#pragma unroll 1
-                for (int e2 = 0; ok && e2 < n_ent; e2++) ok = warp_wait_flag(C, &C.ent_ready[e2]);
+                if (ok) ok = warp_wait_geq(C, &C.staged, n_ent);
                 if (!ok) break;
                 __threadfence_block();
-                float* pb = pbuf + warp * kMaxEnt;
                 // routed experts: epp experts per pass, cpf lanes per expert row
                 const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
                 const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
-                const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
+                if (MAXT == 1) {
+                    // one token, one entry per active expert (entry ent_sorted[a] of expert a, a in
+                    // ascending expert order): the arithmetic of the general case below, in the same
+                    // order, with the per-expert products kept in registers instead of a buffer
+                    const unsigned gm =
+                        L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
+                    float acc = 0.0f;
 #pragma unroll 1
-                for (int s = 0; s < nsub; s++) {
-                    const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
-                    int a0, a1;
-                    down_sub_range(s, na, L, a0, a1);
-                    const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
-#pragma unroll 1
-                    for (int pa = a0; pa < a1; pa += L.epp) {
-                        const int a = pa + al;
-                        if (a < a1) {
-                            const int b = c0 >> 2, u = c0 & 3;
-                            const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
-#pragma unroll 1
-                            for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                                const int ent = C.ent_sorted[j];
+                    for (int s = 0; s < nsub; s++) {
+                        const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
+                        int a0, a1;
+                        down_sub_range(s, na, L, a0, a1);
+                        const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+#pragma unroll 2
+                        for (int pa = a0; pa < a1; pa += L.epp) {
+                            const int a = pa + al;
+                            float pbv = 0.0f;
+                            if (a < a1) {
+                                const int b = c0 >> 2, u = c0 & 3;
+                                const uint8_t* row =
+                                    st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
+                                const int ent = C.ent_sorted[a];
                                 XFrag f;
                                 load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
                                 float v = q2k_chunk_dot(row, u, f);
                                 for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
-                                if (c0 == 0) pb[j] = v * C.hscale[ent];
+                                pbv = v * C.hscale[ent];
+                            }
+                            // the pass's experts, ascending, into lane 0's sum
+#pragma unroll 1
+                            for (int g = 0; g < L.epp; g++) {
+                                const float x = __shfl_sync(0xffffffffu, pbv, g * L.cpf);
+                                if (pa + g < a1) acc = fmaf(C.p[C.ent_sorted[pa + g]], x, acc);
                             }
                         }
                     }
-                }
-                // shared expert down row
-                float sacc[MAXT];
-                if (S > 0)
-                    warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
-                                         reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
-                __syncwarp();
-#pragma unroll
-                for (int t = 0; t < MAXT; t++) {
-                    if (t < T && lane == t) {
-                        float acc = 0.0f;
+                    float sacc[1];
+                    if (S > 0)
+                        warp_dense_row<1>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
+                                          reinterpret_cast<const uint8_t*>(hsf), true, 1, sacc);
+                    if (lane == 0) {
+                        if (S > 0) acc = fmaf(C.gate_s[0], sacc[0], acc);
+                        P.out[r0 + r] = acc;
+                    }
+                } else {
+                    float* pb = pbuf + warp * kMaxEnt;
+                    const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
 #pragma unroll 1
-                        for (int mm = 0; mm < k; mm++) {
-                            const int j = C.tok_sorted[t * k + mm];
-                            acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
+                    for (int s = 0; s < nsub; s++) {
+                        const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
+                        int a0, a1;
+                        down_sub_range(s, na, L, a0, a1);
+                        const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+#pragma unroll 1
+                        for (int pa = a0; pa < a1; pa += L.epp) {
+                            const int a = pa + al;
+                            if (a < a1) {
+                                const int b = c0 >> 2, u = c0 & 3;
+                                const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
+#pragma unroll 1
+                                for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                                    const int ent = C.ent_sorted[j];
+                                    XFrag f;
+                                    load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
+                                    float v = q2k_chunk_dot(row, u, f);
+                                    for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
+                                    if (c0 == 0) pb[j] = v * C.hscale[ent];
+                                }
+                            }
                         }
-                        if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
-                        P.out[(size_t)t * H + r0 + r] = acc;
+                    }
+                    // shared expert down row
+                    float sacc[MAXT];
+                    if (S > 0)
+                        warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
+                                             reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
+                    __syncwarp();
+#pragma unroll
+                    for (int t = 0; t < MAXT; t++) {
+                        if (t < T && lane == t) {
+                            float acc = 0.0f;
+#pragma unroll 1
+                            for (int mm = 0; mm < k; mm++) {
+                                const int j = C.tok_sorted[t * k + mm];
+                                acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
+                            }
+                            if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
+                            P.out[(size_t)t * H + r0 + r] = acc;
+                        }
                     }
                 }
 #pragma unroll 1
@@ -1093,9 +1295,20 @@ static cudaError_t launch_fused_t(const FusedParams& p, size_t smem, DeviceFacts
         f.smem_set[SLOT] = smem;
     }
     FusedParams pp = p;
-    void* args[] = {&pp};
-    // a cooperative launch fails (rather than deadlocks) if the grid cannot be co-resident
-    return cudaLaunchCooperativeKernel(fn, dim3(f.n_sm), dim3(kFusedThreads), args, smem, st);
+    // Not a cooperative launch: that would serialise this call behind the previous one.  The
+    // grid is one CTA per SM and nothing else in the stream runs beside it, so every CTA is
+    // resident; if other work held SMs longer than the wait bound, the call ends in a time-out.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(f.n_sm);
+    cfg.blockDim = dim3(kFusedThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_decode_kernel<MAXT>, pp);
 }
 
 bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err) {

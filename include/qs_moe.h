@@ -168,7 +168,12 @@ int qs_shared_expert_ffn(const qs_moe_shape *shape, const void *x, const qs_shar
  * qs_moe_workspace_bytes(shape, n_tokens) bytes, initialised with
  * qs_workspace_init.  Three implementations, picked per call:
  *  - n_tokens <= 16 and a shape the persistent decode kernel plans for: one
- *    kernel; the result does not depend on how tokens are batched;
+ *    kernel of one CTA per SM that needs every SM at once (other work holding
+ *    SMs for longer than the wait bound ends the call in QS_ERR_TIMEOUT).  It
+ *    is a programmatic dependent launch: it may start while the previous
+ *    kernel in the stream finishes, prefetching weights into L2 meanwhile, and
+ *    waits for that kernel before it reads x or writes anything.  The result
+ *    does not depend on how tokens are batched;
  *  - otherwise, with bf16 x (and Q2_K rows it can stage: hidden a multiple of
  *    1024 or equal to 256; expert_ffn a multiple of 1024 or at most 768): the
  *    tensor-core path -- router on the tensor cores as three exact bf16 planes
