@@ -522,72 +522,6 @@ __device__ __forceinline__ void warp_sort32(float& v, int& i) {
     }
 }
 
-// Compare-exchange of two (value, index) pairs so that slot a holds the one first in key order.
-// Selects, not a conditional swap: a data-dependent branch here diverges the warp and costs
-// several times the arithmetic.
-__device__ __forceinline__ void key_cx(float& va, int& ia, float& vb, int& ib) {
-    const bool sw = key_before(vb, ib, va, ia);
-    const float a = sw ? vb : va, b = sw ? va : vb;
-    const int x = sw ? ib : ia, y = sw ? ia : ib;
-    va = a;
-    vb = b;
-    ia = x;
-    ib = y;
-}
-
-// Sorts the 8 pairs a lane holds into key order (bitonic network, registers only).
-__device__ __forceinline__ void sort8(float (&v)[8], int (&id)[8]) {
-#pragma unroll
-    for (int size = 2; size <= 8; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int m = 0; m < 8; m++) {
-                const int o = m ^ stride;
-                if (o > m) {
-                    if ((m & size) == 0 || size == 8) key_cx(v[m], id[m], v[o], id[o]);
-                    else key_cx(v[o], id[o], v[m], id[m]);
-                }
-            }
-        }
-    }
-}
-
-// One warp: the 8 first entries in key order (larger logit first, then the lower expert id)
-// of E <= 256 logits at `lg`, lane l holding logits l, l + 32, ...  Each lane sorts its 8,
-// then five butterfly steps merge the lane's list with its partner's (the first 8 of two
-// sorted lists: pairwise the better of a[m] and b[7 - m], then a bitonic clean-up), so
-// every lane ends with the same sorted top-8.  A NaN logit ranks below every number.
-__device__ __forceinline__ void warp_top8(const float* lg, int E, float (&v)[8], int (&id)[8]) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int m = 0; m < 8; m++) {
-        const int e = lane + 32 * m;
-        float x = e < E ? ld_relaxed_f32(lg + e) : -INFINITY;
-        v[m] = (x == x) ? x : -INFINITY;
-        id[m] = e < E ? e : 0x7fffffff;
-    }
-    sort8(v, id);
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        float ov[8];
-        int oi[8];
-#pragma unroll
-        for (int m = 0; m < 8; m++) {
-            ov[m] = __shfl_xor_sync(0xffffffffu, v[7 - m], d);
-            oi[m] = __shfl_xor_sync(0xffffffffu, id[7 - m], d);
-        }
-#pragma unroll
-        for (int m = 0; m < 8; m++) key_cx(v[m], id[m], ov[m], oi[m]);
-#pragma unroll
-        for (int stride = 4; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int m = 0; m < 8; m++)
-                if ((m & stride) == 0) key_cx(v[m], id[m], v[m + stride], id[m + stride]);
-        }
-    }
-}
-
 // ------------------------------------------------------------------ the kernel
 
 template <int MAXT>
@@ -672,143 +606,93 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 ok = group_count(2, !got) == 0;
             }
             if (ok) {
-                // small routers (E <= 256, k <= 8): one warp per token, top-k and softmax in registers
-                const bool fast = E <= 256 && k <= 8;
-                if (fast) {
+                // per 32-logit chunk: sort, keep the first k as candidates
+                const int chunks = (E + 31) / 32;
+                const int kc = min(k, 32);
 #pragma unroll 1
-                    for (int t = gwarp; t < T; t += kGW) {
-                        float v[8];
-                        int id[8];
-                        warp_top8(P.xlog + (size_t)t * E, E, v, id);
-                        float den = 0.0f;
-#pragma unroll
-                        for (int m = 0; m < 8; m++)
-                            if (m < k) den += expf(v[m] - v[0]);
-#pragma unroll
-                        for (int m = 0; m < 8; m++) {
-                            if (m < k && lane == m) {
-                                C.ids[t * k + m] = id[m];
-                                C.p[t * k + m] = expf(v[m] - v[0]) / den;
-                                if (T == 1) {
-                                    // one token's k ids are distinct: the rank by id is the grouping
-                                    int rank = 0;
-#pragma unroll
-                                    for (int i = 0; i < 8; i++)
-                                        if (i < k) rank += id[i] < id[m];
-                                    C.ent_sorted[rank] = m;
-                                    C.es[rank] = id[m];
-                                    C.act_e[rank] = id[m];
-                                    C.act_begin[rank] = rank;
-                                    C.tok_sorted[rank] = rank;
-                                }
-                            }
-                        }
-                        if (T == 1 && lane == 0) {
-                            C.act_begin[k] = k;
-                            C.n_active = k;
-                        }
-                    }
-                } else {
-                    // per 32-logit chunk: sort, keep the first k as candidates
-                    const int chunks = (E + 31) / 32;
-                    const int kc = min(k, 32);
-#pragma unroll 1
-                    for (int q = gwarp; q < T * chunks; q += kGW) {
-                        const int t = q / chunks, ch = q % chunks;
-                        const int e = ch * 32 + lane;
-                        float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
-                        if (v != v) v = -INFINITY;  // a NaN logit ranks last
-                        int i = e < E ? e : 0x7fffffff;
-                        warp_sort32(v, i);
-                        if (lane < kc) {
-                            C.cand_v[q * kc + lane] = v;
-                            C.cand_i[q * kc + lane] = i;
-                        }
-                    }
-                    group_sync(2);
-                    // rank among the token's candidates: rank < k is selected
-                    const int nc = chunks * kc;
-#pragma unroll 1
-                    for (int q = gtid; q < T * nc; q += kGT) {
-                        const int t = q / nc;
-                        const float v = C.cand_v[q];
-                        const int i = C.cand_i[q];
-                        int rank = 0;
-#pragma unroll 8
-                        for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
-                        if (rank < k && i < E) {
-                            C.ids[t * k + rank] = i;
-                            C.lsel[t * k + rank] = v;
-                        }
-                    }
-                    group_sync(2);
-                    // softmax over the selected logits (one warp per token)
-#pragma unroll 1
-                    for (int t = gwarp; t < T; t += kGW) {
-                        const float l0 = C.lsel[t * k];
-                        float ex = 0.0f;
-#pragma unroll 1
-                        for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
-                        const float den = warp_sum(ex);
-#pragma unroll 1
-                        for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
+                for (int q = gwarp; q < T * chunks; q += kGW) {
+                    const int t = q / chunks, ch = q % chunks;
+                    const int e = ch * 32 + lane;
+                    float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
+                    if (v != v) v = -INFINITY;  // a NaN logit ranks last
+                    int i = e < E ? e : 0x7fffffff;
+                    warp_sort32(v, i);
+                    if (lane < kc) {
+                        C.cand_v[q * kc + lane] = v;
+                        C.cand_i[q * kc + lane] = i;
                     }
                 }
-                if (fast && T == 1) {
-                    if (gwarp == 0) {
-                        __syncwarp();
-                        if (lane == 0) {
-                            C.et_left = owned_count(L.n_ind, L.n_ind + k * L.tpe, L.G, L.cta) * L.ept;
-                            __threadfence_block();
-                            vstore(&C.routed, 1);
-                        }
-                    }
-                } else {
-                    if (fast) group_sync(2);
-                    // order the entries by (expert, entry)
+                group_sync(2);
+                // rank among the token's candidates: rank < k is selected
+                const int nc = chunks * kc;
 #pragma unroll 1
-                    for (int i = gtid; i < n_ent; i += kGT) {
-                        const int e = C.ids[i];
-                        int rank = 0;
+                for (int q = gtid; q < T * nc; q += kGT) {
+                    const int t = q / nc;
+                    const float v = C.cand_v[q];
+                    const int i = C.cand_i[q];
+                    int rank = 0;
 #pragma unroll 8
-                        for (int j = 0; j < n_ent; j++) {
-                            const int f = C.ids[j];
-                            rank += (f < e) || (f == e && j < i);
-                        }
-                        C.ent_sorted[rank] = i;
-                        C.es[rank] = e;
+                    for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
+                    if (rank < k && i < E) {
+                        C.ids[t * k + rank] = i;
+                        C.lsel[t * k + rank] = v;
                     }
-                    group_sync(2);
-                    // active experts: a run start in es[] opens a new active expert
-                    const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
-                    const unsigned bal = __ballot_sync(0xffffffffu, start);
-                    if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
-                    group_sync(2);
-                    if (gtid < n_ent) {
-                        int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+                }
+                group_sync(2);
+                // softmax over the selected logits (one warp per token)
 #pragma unroll 1
-                        for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
-                        if (start) {
-                            C.act_e[a] = C.es[gtid];
-                            C.act_begin[a] = gtid;
-                        }
-                        if (gtid == n_ent - 1) {
-                            C.act_begin[a + 1] = n_ent;
-                            C.n_active = a + 1;
-                        }
-                        const int t = C.ent_sorted[gtid] / k;
-                        int pos = 0;
+                for (int t = gwarp; t < T; t += kGW) {
+                    const float l0 = C.lsel[t * k];
+                    float ex = 0.0f;
+#pragma unroll 1
+                    for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
+                    const float den = warp_sum(ex);
+#pragma unroll 1
+                    for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
+                }
+                // order the entries by (expert, entry)
+#pragma unroll 1
+                for (int i = gtid; i < n_ent; i += kGT) {
+                    const int e = C.ids[i];
+                    int rank = 0;
 #pragma unroll 8
-                        for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
-                        C.tok_sorted[t * k + pos] = gtid;
+                    for (int j = 0; j < n_ent; j++) {
+                        const int f = C.ids[j];
+                        rank += (f < e) | ((f == e) & (j < i));
                     }
-                    group_sync(2);
-                    if (gtid == 0) {
-                        const int n_et = C.n_active * L.tpe;
-                        C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
-                        __threadfence_block();
-                        vstore(&C.routed, 1);
+                    C.ent_sorted[rank] = i;
+                    C.es[rank] = e;
+                }
+                group_sync(2);
+                // active experts: a run start in es[] opens a new active expert
+                const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
+                const unsigned bal = __ballot_sync(0xffffffffu, start);
+                if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
+                group_sync(2);
+                if (gtid < n_ent) {
+                    int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+#pragma unroll 1
+                    for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
+                    if (start) {
+                        C.act_e[a] = C.es[gtid];
+                        C.act_begin[a] = gtid;
                     }
+                    if (gtid == n_ent - 1) {
+                        C.act_begin[a + 1] = n_ent;
+                        C.n_active = a + 1;
+                    }
+                    const int t = C.ent_sorted[gtid] / k;
+                    int pos = 0;
+#pragma unroll 8
+                    for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
+                    C.tok_sorted[t * k + pos] = gtid;
+                }
+                group_sync(2);
+                if (gtid == 0) {
+                    const int n_et = C.n_active * L.tpe;
+                    C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
+                    __threadfence_block();
+                    vstore(&C.routed, 1);
                 }
             } else {
                 fail(C, status);
@@ -1076,95 +960,49 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 // routed experts: epp experts per pass, cpf lanes per expert row
                 const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
                 const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
-                if (MAXT == 1) {
-                    // one token, one entry per active expert (entry ent_sorted[a] of expert a, a in
-                    // ascending expert order): the arithmetic of the general case below, in the same
-                    // order, with the per-expert products kept in registers instead of a buffer
-                    const unsigned gm =
-                        L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
-                    float acc = 0.0f;
+                float* pb = pbuf + warp * kMaxEnt;
+                const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
 #pragma unroll 1
-                    for (int s = 0; s < nsub; s++) {
-                        const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
-                        int a0, a1;
-                        down_sub_range(s, na, L, a0, a1);
-                        const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
-#pragma unroll 2
-                        for (int pa = a0; pa < a1; pa += L.epp) {
-                            const int a = pa + al;
-                            float pbv = 0.0f;
-                            if (a < a1) {
-                                const int b = c0 >> 2, u = c0 & 3;
-                                const uint8_t* row =
-                                    st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
-                                const int ent = C.ent_sorted[a];
+                for (int s = 0; s < nsub; s++) {
+                    const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
+                    int a0, a1;
+                    down_sub_range(s, na, L, a0, a1);
+                    const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+#pragma unroll 1
+                    for (int pa = a0; pa < a1; pa += L.epp) {
+                        const int a = pa + al;
+                        if (a < a1) {
+                            const int b = c0 >> 2, u = c0 & 3;
+                            const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
+#pragma unroll 1
+                            for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                                const int ent = C.ent_sorted[j];
                                 XFrag f;
                                 load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
                                 float v = q2k_chunk_dot(row, u, f);
                                 for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
-                                pbv = v * C.hscale[ent];
-                            }
-                            // the pass's experts, ascending, into lane 0's sum
-#pragma unroll 1
-                            for (int g = 0; g < L.epp; g++) {
-                                const float x = __shfl_sync(0xffffffffu, pbv, g * L.cpf);
-                                if (pa + g < a1) acc = fmaf(C.p[C.ent_sorted[pa + g]], x, acc);
+                                if (c0 == 0) pb[j] = v * C.hscale[ent];
                             }
                         }
                     }
-                    float sacc[1];
-                    if (S > 0)
-                        warp_dense_row<1>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
-                                          reinterpret_cast<const uint8_t*>(hsf), true, 1, sacc);
-                    if (lane == 0) {
-                        if (S > 0) acc = fmaf(C.gate_s[0], sacc[0], acc);
-                        P.out[r0 + r] = acc;
-                    }
-                } else {
-                    float* pb = pbuf + warp * kMaxEnt;
-                    const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
-#pragma unroll 1
-                    for (int s = 0; s < nsub; s++) {
-                        const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
-                        int a0, a1;
-                        down_sub_range(s, na, L, a0, a1);
-                        const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
-#pragma unroll 1
-                        for (int pa = a0; pa < a1; pa += L.epp) {
-                            const int a = pa + al;
-                            if (a < a1) {
-                                const int b = c0 >> 2, u = c0 & 3;
-                                const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
-#pragma unroll 1
-                                for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                                    const int ent = C.ent_sorted[j];
-                                    XFrag f;
-                                    load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
-                                    float v = q2k_chunk_dot(row, u, f);
-                                    for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
-                                    if (c0 == 0) pb[j] = v * C.hscale[ent];
-                                }
-                            }
-                        }
-                    }
-                    // shared expert down row
-                    float sacc[MAXT];
-                    if (S > 0)
-                        warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
-                                             reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
-                    __syncwarp();
+                }
+                // shared expert down row
+                float sacc[MAXT];
+                if (S > 0)
+                    warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
+                                         reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
+                __syncwarp();
 #pragma unroll
-                    for (int t = 0; t < MAXT; t++) {
-                        if (t < T && lane == t) {
-                            float acc = 0.0f;
+                for (int t = 0; t < MAXT; t++) {
+                    if (t < T && lane == t) {
+                        float acc = 0.0f;
 #pragma unroll 1
-                            for (int mm = 0; mm < k; mm++) {
-                                const int j = C.tok_sorted[t * k + mm];
-                                acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
-                            }
-                            if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
-                            P.out[(size_t)t * H + r0 + r] = acc;
+                        for (int mm = 0; mm < k; mm++) {
+                            const int j = C.tok_sorted[t * k + mm];
+                            acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
                         }
+                        if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
+                        P.out[(size_t)t * H + r0 + r] = acc;
                     }
                 }
 #pragma unroll 1
