@@ -26,16 +26,19 @@
 //     summed in a fixed order (ascending expert id, then the gated shared expert)
 //
 // Cross-CTA exchange: logits, hs and h are plain fp32 arrays in the workspace,
-// each with a completion counter in the workspace header.  A CTA that has
-// written its share of an array (all of its rows of that kind) adds the number
-// of tiles it wrote to the counter with one release reduction; one thread per
-// CTA waits with acquire loads until the counter reaches the array's tile
-// count, and only then does the CTA read the array, once.  (Readers that poll
-// the data words themselves keep the lines being written under a stream of
-// loads, and on this part that delays the writes by microseconds.)  The last
-// CTA to leave zeroes the counters for the next call.  Every wait is bounded
-// by the global timer; a wait that runs out sets the sticky status
-// QS_ERR_TIMEOUT and the CTA winds down.
+// each with a 64-bit completion counter in the workspace header.  A CTA that
+// has written its share of an array (all of its rows of that kind, possibly
+// none) adds 1 to the counter with one release reduction; one thread per CTA
+// waits with acquire loads until the counter reaches this call's target, and
+// only then does the CTA read the array, once.  (Readers that poll the data
+// words themselves keep the lines being written under a stream of loads, and
+// on this part that delays the writes by microseconds.)  The counters are never
+// reset: every call adds exactly gridDim to each of them and to the exit
+// counter (a CTA that winds down early adds what it has not added yet when it
+// leaves), so call n's target is (n + 1) * gridDim, n being the exit count the
+// call finds when it starts divided by gridDim.  Every wait is bounded by the
+// global timer; a wait that runs out sets the sticky status QS_ERR_TIMEOUT and
+// the CTA winds down.
 #include "qs_common.cuh"
 #include "qs_internal.h"
 #include "qs_q2k.cuh"
@@ -82,18 +85,26 @@ struct alignas(16) FusedCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t xbar;  // x and w_sg
+    // one-shot events inside the CTA, waited on with the waiters suspended in hardware
+    uint64_t routed_bar;  // the routing is published
+    uint64_t xq_bar;      // x scales, int16 x and gates are staged
+    uint64_t shared_bar;  // group B has finished its shared gate/up rows (x and w_sg are free)
+    uint64_t hs_bar;      // hs is staged
+    uint64_t h_bar;       // every CTA's h is published
+    uint64_t staged_bar;  // every entry's int16 h is staged (T * k arrivals)
     int done[kMaxStages];  // tasks finished on the tile now in each stage
     int slot_seq[kMaxStages];  // sequence number of the tile a stage is being filled with
-    int routed, xq_ready, hs_ready, abort, issued, n_active, shared_left, h_ready;
+    int abort, issued, n_active, pad1;
     int et_left;   // routed gate/up tasks of this CTA not finished yet
     int h_poller;  // set by the one warp that waits for the h counter
-    int staged;    // entries whose int16 h is staged
-    int pad0;
+    int published; // bit i: this CTA has added its 1 to exchange counter i (kPubLogits, kPubHs, kPubH)
+    uint64_t target;  // this call's target of every exchange counter
     int ids[kMaxEnt];
     float p[kMaxEnt];
     float lsel[kMaxEnt];
     int ent_sorted[kMaxEnt];     // entries t*k+slot sorted by (expert, entry)
     int es[kMaxEnt];             // expert of ent_sorted[i]
+    int es_tok[kMaxEnt];         // token of ent_sorted[i]
     int act_e[kMaxEnt];          // active experts, ascending
     int act_begin[kMaxEnt + 1];  // first ent_sorted index of each active expert
     int tok_sorted[kMaxEnt];     // per token, its k ent_sorted indices, ascending
@@ -139,15 +150,42 @@ __device__ __forceinline__ float4 ld_relaxed_f32x4(const float* p) {
     return v;
 }
 
+// 64-bit exchange counters (gpu scope).
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u64(uint64_t* p, uint64_t v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add_u64(uint64_t* p, uint64_t v) {
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // One thread: wait with acquire loads until the exchange counter *c reaches `target`.
 // False if the CTA is aborting or the wait outlasts kWaitNs.
-__device__ __forceinline__ bool wait_count(const uint32_t* c, uint32_t target, const int* abort) {
-    if (ld_acquire(c) >= target) return true;
+__device__ __forceinline__ bool wait_count(const uint64_t* c, uint64_t target, const int* abort) {
+    if (ld_acquire_u64(c) >= target) return true;
     const uint64_t t0 = global_timer_ns();
-    while (ld_acquire(c) < target) {
+    while (ld_acquire_u64(c) < target) {
         if (*reinterpret_cast<const volatile int*>(abort) || global_timer_ns() - t0 > kWaitNs) return false;
     }
     return true;
+}
+
+enum { kPubLogits = 1, kPubHs = 2, kPubH = 4 };
+
+// One thread: add this CTA's 1 to an exchange counter (release: the CTA's rows of that kind,
+// ordered before this thread by a barrier or a fence, become visible first).
+__device__ __forceinline__ void publish(FusedCtl& C, uint64_t* ctr, int bit) {
+    red_release_add_u64(ctr, 1);
+    atomicOr(&C.published, bit);
 }
 
 // ------------------------------------------------------------------ tile and task bookkeeping
@@ -243,52 +281,20 @@ __device__ __forceinline__ bool warp_wait_tile(FusedCtl& C, int seq, int ns) {
     return __all_sync(0xffffffffu, ok);
 }
 
-// Whole warp waits until *v == 0 (shared memory); false on abort or time-out.
-__device__ __forceinline__ bool warp_wait_zero(FusedCtl& C, const int* v) {
+// Whole warp waits for an mbarrier phase, suspended in hardware between polls (each poll
+// wakes at the latest after 1 us to look at the abort flag); false on abort or time-out.
+__device__ __forceinline__ bool warp_wait_mbar(FusedCtl& C, uint64_t* bar, uint32_t parity) {
     bool ok = true;
-    if (vload(v) != 0) {
+    if (!mbar_try_wait(bar, parity)) {
         const uint64_t t0 = global_timer_ns();
-        while (vload(v) != 0) {
+        while (!mbar_try_wait_sleep(bar, parity, 1000)) {
             if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
                 ok = false;
                 break;
             }
-            __nanosleep(32);
         }
     }
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Whole warp waits until *flag != 0 (shared memory); false on abort or time-out.
-__device__ __forceinline__ bool warp_wait_flag(FusedCtl& C, const int* flag) {
-    bool ok = true;
-    if (!vload(flag)) {
-        const uint64_t t0 = global_timer_ns();
-        while (!vload(flag)) {
-            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
-                ok = false;
-                break;
-            }
-            __nanosleep(32);
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Whole warp waits until *v >= target (shared memory); false on abort or time-out.
-__device__ __forceinline__ bool warp_wait_geq(FusedCtl& C, const int* v, int target) {
-    bool ok = true;
-    if (vload(v) < target) {
-        const uint64_t t0 = global_timer_ns();
-        while (vload(v) < target) {
-            if (vload(&C.abort) || global_timer_ns() - t0 > kWaitNs) {
-                ok = false;
-                break;
-            }
-            __nanosleep(32);
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
+    return __all_sync(0xffffffffu, ok && !vload(&C.abort));
 }
 
 __device__ __forceinline__ void fail(FusedCtl& C, uint32_t* status) {
@@ -390,11 +396,10 @@ __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
         seq++;
     }
     // the routing, published by group A
-    if (!warp_wait_flag(C, &C.routed)) {
+    if (!warp_wait_mbar(C, &C.routed_bar, 0)) {
         if (lane == 0) vstore(&C.abort, 1);
         goto done;
     }
-    __threadfence_block();
     {
         const int na = C.n_active;
         const int n_et = na * L.tpe;
@@ -534,10 +539,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
     const int n_ent = T * k;
     const bool x_f32 = P.x_dtype != QS_BF16;
     uint32_t* status = &P.hdr->status;
-    uint32_t* ctr_exit = &P.hdr->ctr[kCtrExit][0];
-    uint32_t* ctr_lg = &P.hdr->ctr[kCtrLogits][0];
-    uint32_t* ctr_hs = &P.hdr->ctr[kCtrHs][0];
-    uint32_t* ctr_h = &P.hdr->ctr[kCtrH][0];
+    uint64_t* ctr_exit = reinterpret_cast<uint64_t*>(&P.hdr->ctr[kCtrExit][0]);
+    uint64_t* ctr_lg = reinterpret_cast<uint64_t*>(&P.hdr->ctr[kCtrLogits][0]);
+    uint64_t* ctr_hs = reinterpret_cast<uint64_t*>(&P.hdr->ctr[kCtrHs][0]);
+    uint64_t* ctr_h = reinterpret_cast<uint64_t*>(&P.hdr->ctr[kCtrH][0]);
     const uint8_t* xraw = data;                                              // [T x H] as given
     uint32_t* xqf = reinterpret_cast<uint32_t*>(data + P.off_xq);            // [T][H/64 chunks][36] fragments
     const uint8_t* sigbuf = data + P.off_sig;                                // [H] bf16
@@ -555,12 +560,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             C.slot_seq[i] = -1;
         }
         mbar_init(&C.xbar, 1);
-        C.routed = C.xq_ready = C.hs_ready = C.h_ready = C.abort = C.issued = C.n_active = 0;
-        C.et_left = C.h_poller = C.staged = 0;
-        {
-            const Plan L0 = make_plan(P);
-            C.shared_left = L0.own_st * P.RS;  // shared gate/up row tasks of this CTA
-        }
+        mbar_init(&C.routed_bar, 1);
+        mbar_init(&C.xq_bar, 1);
+        mbar_init(&C.shared_bar, 1);
+        mbar_init(&C.hs_bar, 1);
+        mbar_init(&C.h_bar, 1);
+        mbar_init(&C.staged_bar, (uint32_t)(P.T * P.k));
+        C.abort = C.issued = C.n_active = 0;
+        C.et_left = C.h_poller = C.published = 0;
+        C.target = 0;
         fence_barrier_init();
     }
     __syncthreads();
@@ -570,6 +578,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         producer(P, C, data);
     } else {
         asm volatile("griddepcontrol.wait;" ::: "memory");
+        // every earlier call has left (the wait above), none of this call can leave before this
+        // CTA publishes its logits: the exit count is an exact multiple of gridDim here
+        if (tid == 0) C.target = (ld_relaxed_u64(ctr_exit) / gridDim.x + 1) * gridDim.x;
         const Plan L = make_plan(P);
         const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
         bool ok = warp_wait_bar(C, &C.xbar, 0);
@@ -600,8 +611,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             if (ok) {
                 bool got = true;
                 if (gtid == 0) {
-                    if (L.own_rt > 0) red_release_add(ctr_lg, (uint32_t)L.own_rt);
-                    got = wait_count(ctr_lg, (uint32_t)L.n_rt, &C.abort);
+                    publish(C, ctr_lg, kPubLogits);
+                    got = wait_count(ctr_lg, C.target, &C.abort);
                 }
                 ok = group_count(2, !got) == 0;
             }
@@ -623,17 +634,23 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                 }
                 group_sync(2);
-                // rank among the token's candidates: rank < k is selected
+                // rank among the token's candidates: rank < k is selected.  Four adjacent lanes
+                // share a candidate, each counting a quarter of the others.
                 const int nc = chunks * kc;
+                const int n4 = T * nc * 4;
 #pragma unroll 1
-                for (int q = gtid; q < T * nc; q += kGT) {
+                for (int q4 = gtid; q4 < (n4 + 31) / 32 * 32; q4 += kGT) {
+                    const bool live = q4 < n4;
+                    const int q = live ? q4 >> 2 : 0, part = q4 & 3;
                     const int t = q / nc;
                     const float v = C.cand_v[q];
                     const int i = C.cand_i[q];
                     int rank = 0;
-#pragma unroll 8
-                    for (int j = 0; j < nc; j++) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
-                    if (rank < k && i < E) {
+#pragma unroll 4
+                    for (int j = part; j < nc; j += 4) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
+                    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+                    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+                    if (live && part == 0 && rank < k && i < E) {
                         C.ids[t * k + rank] = i;
                         C.lsel[t * k + rank] = v;
                     }
@@ -662,6 +679,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                     C.ent_sorted[rank] = i;
                     C.es[rank] = e;
+                    C.es_tok[rank] = i / k;
                 }
                 group_sync(2);
                 // active experts: a run start in es[] opens a new active expert
@@ -681,18 +699,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         C.act_begin[a + 1] = n_ent;
                         C.n_active = a + 1;
                     }
-                    const int t = C.ent_sorted[gtid] / k;
+                    const int t = C.es_tok[gtid];
                     int pos = 0;
 #pragma unroll 8
-                    for (int j = 0; j < gtid; j++) pos += C.ent_sorted[j] / k == t;
+                    for (int j = 0; j < gtid; j++) pos += C.es_tok[j] == t;
                     C.tok_sorted[t * k + pos] = gtid;
                 }
                 group_sync(2);
                 if (gtid == 0) {
                     const int n_et = C.n_active * L.tpe;
                     C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
-                    __threadfence_block();
-                    vstore(&C.routed, 1);
+                    if (C.et_left == 0) publish(C, ctr_h, kPubH);  // no routed rows here
+                    mbar_arrive(&C.routed_bar);
                 }
             } else {
                 fail(C, status);
@@ -773,10 +791,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                 }
                 group_sync(3);
-                if (gtid == 0) {
-                    __threadfence_block();
-                    vstore(&C.xq_ready, 1);
-                }
+                if (gtid == 0) mbar_arrive(&C.xq_bar);
             } else {
                 fail(C, status);
             }
@@ -795,16 +810,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int t = 0; t < MAXT; t++)
                     if (t < T && lane == t) P.xhs[(size_t)t * S + j * P.RS + r] = silu(ga[t]) * ua[t];
                 release_slot(C, sq % ns, P.RS);
-                if (lane == 0) atomicSub(&C.shared_left, 1);
             }
             if (!ok) fail(C, status);
             // every hs row of this CTA is stored: publish them (the barrier orders the stores)
-            if (group_count(3, !ok) == 0 && gtid == 0 && L.own_st > 0) red_release_add(ctr_hs, (uint32_t)L.own_st);
+            if (group_count(3, !ok) == 0 && gtid == 0) {
+                publish(C, ctr_hs, kPubHs);
+                mbar_arrive(&C.shared_bar);
+            }
         }
 
         // ---------------------------------------------------------- every warp: the routed part
-        if (ok && !(ok = warp_wait_flag(C, &C.routed))) fail(C, status);
-        __threadfence_block();
+        if (ok && !(ok = warp_wait_mbar(C, &C.routed_bar, 0))) fail(C, status);
         const int na = ok ? C.n_active : 0;
         const int n_et = na * L.tpe;
         const int own_et = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta);
@@ -822,8 +838,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             if (q < q_et) {
                 // ---------------------------------------------- routed gate/up rows
                 if (!xq_seen) {
-                    if (!(ok = warp_wait_flag(C, &C.xq_ready))) break;
-                    __threadfence_block();
+                    if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
                     xq_seen = true;
                 }
                 const int m = q / L.ept, rt = q % L.ept;
@@ -868,19 +883,18 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     __threadfence_block();
                     if (atomicSub(&C.et_left, 1) == 1) {
                         __threadfence_block();
-                        red_release_add(ctr_h, (uint32_t)own_et);
+                        publish(C, ctr_h, kPubH);
                     }
                 }
             } else if (q < q_et + n_stage_tasks) {
                 // ---------------------------------------------- staging of hs / of one entry's int16 h
                 const int sidx = q - q_et;
                 // the int16 h cache aliases x and w_sg: wait until their last reader is done
-                if (!(ok = warp_wait_flag(C, &C.xq_ready))) break;
-                if (!(ok = warp_wait_zero(C, &C.shared_left))) break;
-                __threadfence_block();
+                if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
+                if (!(ok = warp_wait_mbar(C, &C.shared_bar, 0))) break;
                 if (S > 0 && sidx == 0) {
                     int got = 1;
-                    if (lane == 0) got = wait_count(ctr_hs, (uint32_t)L.n_st, &C.abort);
+                    if (lane == 0) got = wait_count(ctr_hs, C.target, &C.abort);
                     got = __shfl_sync(0xffffffffu, got, 0);
                     __syncwarp();
                     if (!(ok = got != 0)) break;
@@ -888,24 +902,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     for (int i = lane * 4; i < T * S; i += 128)
                         *reinterpret_cast<float4*>(hsf + i) = ld_relaxed_f32x4(P.xhs + i);
                     __syncwarp();
-                    if (lane == 0) {
-                        __threadfence_block();
-                        vstore(&C.hs_ready, 1);
-                    }
+                    if (lane == 0) mbar_arrive(&C.hs_bar);
                 } else {
                     const int ent = sidx - (S > 0 ? 1 : 0);
                     // the first entry task to get here waits for the h counter; the others for its flag
                     int got = 1;
                     if (lane == 0 && atomicCAS(&C.h_poller, 0, 1) == 0) {
-                        got = wait_count(ctr_h, (uint32_t)n_et, &C.abort);
-                        if (got) {
-                            __threadfence_block();
-                            vstore(&C.h_ready, 1);
-                        }
+                        got = wait_count(ctr_h, C.target, &C.abort);
+                        if (got) mbar_arrive(&C.h_bar);
                     }
                     got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!(ok = got != 0 && warp_wait_flag(C, &C.h_ready))) break;
-                    __threadfence_block();
+                    if (!(ok = got != 0 && warp_wait_mbar(C, &C.h_bar, 0))) break;
                     const float* hr = P.xh + (size_t)ent * F;
                     // lane: 8 consecutive values per 256; one pass for the scale, one to quantise
                     float m = 0.0f;
@@ -939,10 +946,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                     if (lane == 0) C.hscale[ent] = m * (1.0f / 32767.0f);
                     __syncwarp();
-                    if (lane == 0) {
-                        __threadfence_block();
-                        atomicAdd(&C.staged, 1);
-                    }
+                    if (lane == 0) mbar_arrive(&C.staged_bar);
                 }
             } else {
                 // ---------------------------------------------- one down row
@@ -953,10 +957,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const int sq0 = seq_dg + m * nsub;
 #pragma unroll 1
                 for (int s = 0; ok && s < nsub; s++) ok = warp_wait_tile(C, sq0 + s, ns);
-                if (ok && S > 0) ok = warp_wait_flag(C, &C.hs_ready);
-                if (ok) ok = warp_wait_geq(C, &C.staged, n_ent);
+                if (ok && S > 0) ok = warp_wait_mbar(C, &C.hs_bar, 0);
+                if (ok) ok = warp_wait_mbar(C, &C.staged_bar, 0);
                 if (!ok) break;
-                __threadfence_block();
                 // routed experts: epp experts per pass, cpf lanes per expert row
                 const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
                 const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
@@ -1021,15 +1024,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             if (!mbar_wait(&C.full[s % ns], (s / ns) & 1)) set_status(status, QS_ERR_TIMEOUT);
         if (!mbar_wait(&C.xbar, 0)) set_status(status, QS_ERR_TIMEOUT);
         if (vload(&C.abort)) set_status(status, QS_ERR_TIMEOUT);
-        const uint32_t old = atom_acq_rel_add(ctr_exit, 1u);
-        if (old == gridDim.x - 1) {
-            // last CTA out: every CTA is past its last counter wait; zero the counters for the next call
-            *reinterpret_cast<volatile uint32_t*>(ctr_lg) = 0u;
-            *reinterpret_cast<volatile uint32_t*>(ctr_hs) = 0u;
-            *reinterpret_cast<volatile uint32_t*>(ctr_h) = 0u;
-            *reinterpret_cast<volatile uint32_t*>(ctr_exit) = 0u;
-            __threadfence();
-        }
+        // keep every counter at exactly gridDim per call, whatever happened
+        const int pub = vload(&C.published);
+        if (!(pub & kPubLogits)) red_relaxed_add_u64(ctr_lg, 1);
+        if (!(pub & kPubHs)) red_relaxed_add_u64(ctr_hs, 1);
+        if (!(pub & kPubH)) red_relaxed_add_u64(ctr_h, 1);
+        red_relaxed_add_u64(ctr_exit, 1);
     }
 }
 
