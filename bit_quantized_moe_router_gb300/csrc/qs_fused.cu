@@ -13,8 +13,13 @@
 // be refilled.  Tiles, in the order every CTA walks them (tile i of the grid
 // belongs to CTA i mod gridDim):
 //
-//   router rows (fp32)  |  shared gate/up rows (bf16)  |  routed gate/up rows (Q2_K)  |  down groups
+//   router rows (fp32)  |  shared gate/up rows (bf16)  |  [routed gate/up rows (Q2_K)]  |  down groups
 //
+// The routed gate/up rows are numbered as tiles but do not pass through the ring:
+// the warps that use them load them from global memory into registers, after
+// each warp has requested all of its rows into L2 at once (one SM's copy engine
+// works through its copies one after another; the load path keeps far more of
+// them in flight).
 // Consumers work as independent warp tasks, so different warps can be in
 // different phases at once and nothing waits on a CTA-wide barrier:
 //   group A (warps 0-7):  router rows -> logits; then the routing
@@ -405,23 +410,6 @@ __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
         const int n_et = na * L.tpe;
         const int lo_dg = L.n_ind + n_et, hi_dg = lo_dg + L.n_dg;
         const int64_t down_off = 2ll * P.F * L.rowH;
-        // routed gate/up rows: the critical path, issued first
-#pragma unroll 1
-        for (int g = first_owned(L.n_ind, L.G, L.cta); g < L.n_ind + n_et; g += L.G) {
-            if (!producer_slot(C, seq, ns)) goto done;
-            const int idx = g - L.n_ind;
-            const int a = idx / L.tpe, tt = idx % L.tpe;
-            const uint8_t* gate = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)tt * P.R * L.rowH;
-            const uint32_t bytes = (uint32_t)P.R * L.rowH;
-            if (lane == 0) mbar_arrive_expect_tx(bar(seq), 2 * bytes);
-            __syncwarp();
-            if (lane < 2) {
-                fence_proxy_async_smem();
-                bulk_g2s(slot(seq) + lane * bytes, gate + (int64_t)lane * P.F * L.rowH, bytes, bar(seq));
-            }
-            __syncwarp();
-            seq++;
-        }
         // down groups: nsub consecutive stages each
         const int nsub = down_subtiles(na, L);
 #pragma unroll 1
@@ -828,11 +816,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int own_dg = owned_count(lo_dg, lo_dg + L.n_dg, L.G, L.cta);
         const int nsub = down_subtiles(na, L);
         const int seq_et = L.own_rt + L.own_st;       // stage sequence number of the first routed tile
-        const int seq_dg = seq_et + own_et;           // ... of the first down group
+        const int seq_dg = seq_et;                    // ... of the first down group (routed rows bypass the ring)
         const int n_stage_tasks = (S > 0 ? 1 : 0) + n_ent;
         const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
         const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
         bool xq_seen = false;
+        // every routed gate/up row this warp will read, requested at once (lines into L2)
+#pragma unroll 1
+        for (int q = warp; ok && q < q_et; q += kCW) {
+            const int m = q / L.ept, rt = q % L.ept;
+            const int idx = first_owned(L.n_ind, L.G, L.cta) + m * L.G - L.n_ind;
+            const int a = idx / L.tpe, tt = idx % L.tpe;
+            const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw) * L.rowH;
+            const int lines = (L.rpw * L.rowH + 127) / 128;  // rows of the task are contiguous
+#pragma unroll 1
+            for (int l = lane; l < 2 * lines; l += 32) {
+                const uint8_t* p = row0 + (l >= lines ? (int64_t)P.F * L.rowH : 0) + (int64_t)(l % lines) * 128;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            }
+        }
 #pragma unroll 1
         for (int q = warp; ok && q < q_all; q += kCW) {
             if (q < q_et) {
@@ -842,18 +844,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     xq_seen = true;
                 }
                 const int m = q / L.ept, rt = q % L.ept;
-                const int sq = seq_et + m;
                 const int g = first_owned(L.n_ind, L.G, L.cta) + m * L.G;
                 const int idx = g - L.n_ind;
                 const int a = idx / L.tpe, tt = idx % L.tpe;
-                if (!(ok = warp_wait_tile(C, sq, ns))) break;
-                const uint8_t* st = stages + (size_t)(sq % ns) * kStageBytes;
                 // lanes: (row within the task, chunk); long rows: each lane walks several chunks
                 const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
                 const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
                 const int cstep = L.cpr >= 32 ? 32 : L.cpr;
                 const int r = rt * L.rpw + rl;
                 const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
+                // the rows come straight from global memory into registers: every warp's loads are
+                // in flight at once, instead of queueing in the SM's copy engine one tile after another
+                const uint8_t* grow = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + r) * L.rowH;
+                const uint8_t* urow = grow + (int64_t)P.F * L.rowH;
 #pragma unroll 1
                 for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
                     const int ent = C.ent_sorted[j];
@@ -864,9 +867,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         const int b = c >> 2, u = c & 3;
                         XFrag f;
                         load_xfrag_f(xqf + ((size_t)t * (H / 64) + c) * kFragWords, f);
-                        const uint8_t* grow = st + (size_t)r * L.rowH + b * kBlockBytes;
-                        gv += q2k_chunk_dot(grow, u, f);
-                        uv += q2k_chunk_dot(grow + (size_t)P.R * L.rowH, u, f);
+                        Q2Chunk gc, uc;
+                        load_q2chunk_global(grow + b * kBlockBytes, u, gc);
+                        load_q2chunk_global(urow + b * kBlockBytes, u, uc);
+                        gv += q2k_chunk_dot(gc, u, f);
+                        uv += q2k_chunk_dot(uc, u, f);
                     }
                     for (int o = min(L.cpr, 32) >> 1; o > 0; o >>= 1) {
                         gv += __shfl_xor_sync(gm, gv, o);
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
                     }
                 }
-                release_slot(C, sq % ns, L.ept);  // (its __syncwarp orders the lanes' h stores)
+                __syncwarp();  // orders the lanes' h stores before lane 0's fences below
                 // the CTA's last routed task publishes all of the CTA's h tiles
                 if (lane == 0) {
                     __threadfence_block();

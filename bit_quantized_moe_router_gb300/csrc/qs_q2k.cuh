@@ -118,16 +118,36 @@ __device__ __forceinline__ void frag_pos(int p, int& word, int& half) {
     half = e & 1;
 }
 
-// Partial dot of chunk u of the block at blk (shared memory, 4-byte aligned)
-// with the thread's activations: d * sum sc_lo*S - dmin * sum sc_hi*X (unscaled by s_x).
-__device__ __forceinline__ float q2k_chunk_dot(const uint8_t* blk, int u, const XFrag& f) {
-    const uint32_t* b32 = reinterpret_cast<const uint32_t*>(blk);
-    const int h = u >> 1;
+// The words of one Q2_K block that chunk u reads: its 16 quant bytes, the 8 scale bytes of
+// its half, and d | dmin.
+struct Q2Chunk {
     uint32_t q[4];
+    uint32_t sca, scb, dd;
+};
+
+// Chunk u of the block at blk (4-byte aligned; shared or global memory).
+__device__ __forceinline__ void load_q2chunk(const uint8_t* blk, int u, Q2Chunk& c) {
+    const uint32_t* b32 = reinterpret_cast<const uint32_t*>(blk);
 #pragma unroll
-    for (int w = 0; w < 4; w++) q[w] = b32[4 + 4 * u + w];
-    const uint32_t sca = b32[2 * h], scb = b32[2 * h + 1];
-    const uint32_t dd = b32[20];
+    for (int w = 0; w < 4; w++) c.q[w] = b32[4 + 4 * u + w];
+    c.sca = b32[2 * (u >> 1)];
+    c.scb = b32[2 * (u >> 1) + 1];
+    c.dd = b32[20];
+}
+
+// The same words from global memory through the read-only path.
+__device__ __forceinline__ void load_q2chunk_global(const uint8_t* blk, int u, Q2Chunk& c) {
+    const uint32_t* b32 = reinterpret_cast<const uint32_t*>(blk);
+#pragma unroll
+    for (int w = 0; w < 4; w++) c.q[w] = __ldg(b32 + 4 + 4 * u + w);
+    c.sca = __ldg(b32 + 2 * (u >> 1));
+    c.scb = __ldg(b32 + 2 * (u >> 1) + 1);
+    c.dd = __ldg(b32 + 20);
+}
+
+// Partial dot of chunk u of a block (its words in c) with the thread's activations:
+// d * sum sc_lo*S - dmin * sum sc_hi*X (unscaled by s_x).
+__device__ __forceinline__ float q2k_chunk_dot(const Q2Chunk& c, int u, const XFrag& f) {
     const int sh0 = 8 * (u & 1);
     int plo = 0, phi = 0;
 #pragma unroll
@@ -136,18 +156,25 @@ __device__ __forceinline__ float q2k_chunk_dot(const uint8_t* blk, int u, const 
         int t = 0;
 #pragma unroll
         for (int w = 0; w < 4; w++) {
-            const uint32_t v = q[w] & mask;
+            const uint32_t v = c.q[w] & mask;
             t = dp2a_lo(f.v[j][w][0], v, t);
             t = dp2a_hi(f.v[j][w][1], v, t);
         }
         t >>= 2 * j;
-        const uint32_t sc = ((j < 2 ? sca : scb) >> (sh0 + 16 * (j & 1))) & 0xffu;
+        const uint32_t sc = ((j < 2 ? c.sca : c.scb) >> (sh0 + 16 * (j & 1))) & 0xffu;
         plo += (int)(sc & 15u) * t;
         phi += (int)(sc >> 4) * f.xs[j];
     }
-    const float d = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu)));
-    const float dm = __half2float(__ushort_as_half((unsigned short)(dd >> 16)));
+    const float d = __half2float(__ushort_as_half((unsigned short)(c.dd & 0xffffu)));
+    const float dm = __half2float(__ushort_as_half((unsigned short)(c.dd >> 16)));
     return __fmaf_rn(d, (float)plo, __fmul_rn(-dm, (float)phi));
+}
+
+// Partial dot of chunk u of the block at blk (shared memory, 4-byte aligned).
+__device__ __forceinline__ float q2k_chunk_dot(const uint8_t* blk, int u, const XFrag& f) {
+    Q2Chunk c;
+    load_q2chunk(blk, u, c);
+    return q2k_chunk_dot(c, u, f);
 }
 
 
