@@ -66,6 +66,7 @@ def lib():
             L.qso_moe_ffn.restype = i32
             L.qso_moe_ffn.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, i32, P, P, P, i64,
                                       P, P, P, P, P, P, P, P, P, P, P]
+            L.qso_steer_rows.argtypes = [i32, i32, P, ctypes.c_double, P]
             _lib = L
     return _lib
 
@@ -244,3 +245,18 @@ def moe_ffn(shape, x, Wr, bias, experts, expert_stride, shared, tokens=None, thr
     if errors:
         raise ValueError(f"qso_moe_ffn failed ({errors[0]})")
     return {"ids": ids, "p": p, "margin": margin, "y": y, "h": h, "hs": hs[:, :S], "gate": gate}
+
+
+def steer_rows(y, d, scale):
+    """Directional steering of FFN output rows, y <- y - scale * d * (d . y), per row.
+
+    QuarkStar (q36) README, "Steering".  y: [T, H] (any float type, widened to
+    double); d: [H] fp32 direction (used as given); returns a new [T, H] float64.
+    """
+    yy = np.array(y, dtype=np.float64, order="C").reshape(-1, np.shape(y)[-1]).copy()
+    T, H = yy.shape
+    dd = _c(d, np.float32).reshape(-1)
+    if dd.shape[0] != H:
+        raise ValueError("direction length differs from the row length")
+    lib().qso_steer_rows(H, T, _p(dd), float(scale), _p(yy))
+    return yy

@@ -365,3 +365,24 @@ int qso_moe_ffn(int H, int E, int k, int F, int S, int t0, int nt, const void *x
     free(xw); free(h); free(ye); free(hs);
     return rc;
 }
+
+/* ------------------------------------------------------------------ */
+/* directional steering of the FFN output                               */
+/* ------------------------------------------------------------------ */
+
+/* QuarkStar (q36) README, "Steering" (the same projection as DwarfStar's
+ * "Steering" section): every token's FFN output row is edited in place as
+ *     y <- y - scale * d * (d . y)
+ * with d the layer's direction (stored normalised; this function does not
+ * normalise it) and scale a scalar: positive removes the direction, negative
+ * amplifies it, zero leaves y unchanged.  y: [T x H] double, d: [H] fp32
+ * widened exactly.  The dot is taken first for the whole row, then the row
+ * is updated, in the order of the formula. */
+void qso_steer_rows(int H, int T, const float *d, double scale, double *y) {
+    for (int t = 0; t < T; t++) {
+        double *yt = y + (size_t)t * H;
+        double c = 0.0;
+        for (int i = 0; i < H; i++) c += (double)d[i] * yt[i];
+        for (int i = 0; i < H; i++) yt[i] = yt[i] - scale * (double)d[i] * c;
+    }
+}
