@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--max-copies", type=int, default=48)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--steer", type=float, default=0.0,
+                    help="directional steering of every output row with this scale (0: off)")
     return ap.parse_args()
 
 
@@ -291,7 +293,8 @@ def config_of(w, T, args):
             "l2": ("inputs larger than L2: %d layer copies cycled, no flush" % getattr(args, "copies_used", w.copies))
                   if args.l2 == "cycle" else
                   "flushed between timed steps (512 MiB write + 256 MiB read, outside the events)",
-            "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+            "parallelism": "replicas" if args.gpus > 1 else "single GPU",
+            **({"steer_scale": args.steer} if args.steer else {})}
 
 
 # ------------------------------------------------------------------ our arm
@@ -352,6 +355,9 @@ def run_ours(args, w, T):
     launches_per_step = qm.qs_moe_ffn_launches(shape, T, True)
     if launches_per_step < 1:
         raise SystemExit(f"qs_moe_ffn_launches failed ({launches_per_step})")
+    layer_launches = launches_per_step
+    if args.steer:
+        launches_per_step += 1  # qs_steer_rows after the layer
 
     # copies: the workload's own count, or enough that nothing a step reads is still in L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -377,10 +383,14 @@ def run_ours(args, w, T):
         j = (i * T) % qi.X_POOL
         return xdev[j:j + T]
 
+    direction = torch.from_numpy(qi.gen_direction(H, w.seed)).to(device)
+
     def step(i, x=None, n_layers=None):
         Ld = layers[i % (n_layers or len(layers))]
         qm.qs_moe_ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T,
                       ws, stream)
+        if args.steer:
+            qm.qs_steer_rows(out, direction, args.steer, T, stream)
 
     # distinct experts per step (routing is a function of the copy and the x rows)
     ids = torch.empty((T, sh.top_k), dtype=torch.int32, device=device)
@@ -468,9 +478,26 @@ def run_ours(args, w, T):
     torch.cuda.synchronize()
     e2e_s = dist.max(e2e_a.elapsed_time(e2e_b) / 1e3)
 
+    steer = None
+    if args.steer:
+        torch.cuda.synchronize()
+        sa, sb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(3):
+            qm.qs_steer_rows(out, direction, args.steer, T, stream)
+        sa.record(stream)
+        for _ in range(K):
+            qm.qs_steer_rows(out, direction, args.steer, T, stream)
+        sb.record(stream)
+        torch.cuda.synchronize()
+        s_us = sa.elapsed_time(sb) / K * 1e3
+        s_bytes = 2 * T * H * 4 + H * 4
+        steer = {"kernel": "steer_rows_kernel", "us_per_call": s_us, "bytes_per_call": s_bytes,
+                 "achieved_gbs": s_bytes / (s_us * 1e-6) / 1e9,
+                 "note": "qs_steer_rows alone, K back-to-back calls on the layer's output rows (L2-resident)"}
+
     # roofline of the layer kernel: algorithmic bytes over the measured step time
     algo = [algorithmic_bytes(sh, T, distinct[(args.warmup + j) % period]) for j in range(K)]
-    algo_bytes = float(np.mean([a for a, _ in algo]))
+    algo_bytes = float(np.mean([a for a, _ in algo])) + (H * 4 if args.steer else 0)
     q2k_bytes = float(np.mean([q for _, q in algo]))
     mean_step_s = total_s / K
     pk = peaks()
@@ -488,22 +515,23 @@ def run_ours(args, w, T):
                "sample": f"{calls} layer calls of {ts} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
                          f"the experts they route to" + (" (per-token cost independent of the batch)" if T > ts else "")
                          + f"; {cpu_model()}"}
-    if launches_per_step > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
+    if layer_launches > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
         flops = layer_flops(sh, T)
         tf_peak = pk["bf16_tflops"] if pk else 1900.0
         tf = flops / mean_step_s / 1e12
-        roof = {"bound": "tensor", "kernel": "qs_moe_ffn (whole layer, %d kernels)" % launches_per_step,
+        roof = {"bound": "tensor", "kernel": "qs_moe_ffn (whole layer, %d kernels)" % layer_launches,
                 "achieved": tf, "peak": tf_peak, "unit": "TFLOP/s", "frac": tf / tf_peak,
                 "peak_source": ("MEASURED_PEAKS.json bf16_tflops, dense 16-bit burst (fp16 runs at the bf16 rate; "
                                 "of measured)") if pk else "fallback 1.9 PFLOP/s",
                 "algorithmic_flops_per_launch": flops, "traffic": None}
     else:
         roof = {"bound": "hbm",
-                "kernel": "fused_decode_kernel" if launches_per_step == 1 else "qs_moe_ffn (whole layer)",
+                "kernel": "fused_decode_kernel" if layer_launches == 1 else "qs_moe_ffn (whole layer)",
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
                 "algorithmic_bytes_per_launch": algo_bytes,
-                "traffic": recorded_traffic(w.name) if launches_per_step == 1 and T == w.tokens[0] else None}
+                "traffic": recorded_traffic(w.name) if layer_launches == 1 and T == w.tokens[0] and not args.steer
+                else None}
     line = {
         "metric": metric_name(T),
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
@@ -524,6 +552,7 @@ def run_ours(args, w, T):
         "clocks": clk,
         "bracket_wall_s": wall,
         "cpu_baseline": cpu,
+        **({"steer": steer} if steer else {}),
     }
     print(json.dumps(line), flush=True)
 

@@ -260,6 +260,14 @@ int qs_q2k_quantize(const float* w, int64_t n_rows, int64_t K, void* out, void* 
     return e == cudaSuccess ? QS_OK : cuda_fail(e);
 }
 
+int qs_steer_rows(float* out, const float* direction, float scale, int n_tokens, int hidden, void* stream) {
+    if (!out || !direction || n_tokens < 1 || hidden < 4 || hidden % 4 || !aligned16(out) || !aligned16(direction))
+        return QS_ERR_INVALID;
+    if (scale == 0.0f) return QS_OK;
+    cudaError_t e = launch_steer_rows(out, direction, scale, n_tokens, hidden, (cudaStream_t)stream);
+    return e == cudaSuccess ? QS_OK : cuda_fail(e);
+}
+
 int qs_test_wait_timeout(void* workspace, size_t workspace_bytes, int limit_us, void* stream) {
     if (!workspace || workspace_bytes < (size_t)kHeaderBytes || ((uintptr_t)workspace & 255u) || limit_us < 1 ||
         limit_us > 1000000)

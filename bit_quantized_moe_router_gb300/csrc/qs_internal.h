@@ -57,6 +57,9 @@ cudaError_t launch_shared_gateup(const qs_moe_shape& s, const void* x, const uin
 cudaError_t launch_quantize(const float* w, int64_t n_blocks, uint8_t* out, cudaStream_t st);
 cudaError_t launch_test_wait(void* ws, uint64_t limit_ns, cudaStream_t st);
 
+// Directional steering of output rows (qs_steer.cu): y <- y - scale * d * (d . y) per row.
+cudaError_t launch_steer_rows(float* y, const float* d, float scale, int T, int H, cudaStream_t st);
+
 // Persistent single-kernel decode path (qs_fused.cu).  cudaErrorNotSupported
 // when the shape or token count is outside its plan; the caller then runs the
 // per-step kernels.  sg == nullptr means no shared expert.

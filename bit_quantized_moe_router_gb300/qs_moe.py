@@ -22,7 +22,7 @@ EXPORTS = (
     "qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes", "qs_workspace_init",
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
     "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
-    "qs_moe_ffn_noalloc",
+    "qs_moe_ffn_noalloc", "qs_steer_rows",
 )
 
 
@@ -85,6 +85,7 @@ def load(build_if_missing: bool = True):
     L.qs_moe_ffn_noalloc.argtypes = [SP, P, P, P, EP, HP, P, i32, P]
     L.qs_q2k_quantize.argtypes = [P, i64, i64, P, P]
     L.qs_test_wait_timeout.argtypes = [P, sz, i32, P]
+    L.qs_steer_rows.argtypes = [P, P, ctypes.c_float, i32, i32, P]
     for name in EXPORTS:
         if name not in ("qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes"):
             getattr(L, name).restype = i32
@@ -197,6 +198,12 @@ def qs_moe_ffn_noalloc(shape, x, router_w, router_bias, experts: qs_q2k_experts,
     _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
                                      ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
                                      _ptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
+
+
+def qs_steer_rows(out, direction, scale, n_tokens, stream=None):
+    """In place, per row of out [n_tokens, hidden] fp32: y <- y - scale * direction * (direction . y)."""
+    _check(load().qs_steer_rows(_ptr(out), _ptr(direction), float(scale), n_tokens, out.shape[-1],
+                                _stream(stream)), "qs_steer_rows")
 
 
 def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:

@@ -205,6 +205,20 @@ int qs_moe_ffn_noalloc(const qs_moe_shape *shape, const void *x, const float *ro
                        const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                        void *stream);
 
+/* Directional steering of the layer's output, in place (QuarkStar (q36)
+ * README, "Steering"; DwarfStar (ds4) page, "Steering"): every token row
+ * y of out is replaced by y - scale * direction * (direction . y).
+ * out: device fp32 [n_tokens x hidden], row-major, the rows a qs_moe_ffn call
+ * wrote (or any rows); direction: device fp32 [hidden], the layer's
+ * direction as stored (normalised by the caller; the library does not
+ * normalise it).  Positive scale removes the direction, negative amplifies
+ * it; scale == 0 is the unsteered path and launches nothing.  hidden must be a
+ * positive multiple of 4 and both pointers 16-byte aligned; otherwise
+ * QS_ERR_INVALID before any launch.  One kernel on `stream`, one CTA per row,
+ * the dot product summed in a fixed order (run-to-run identical).  The caller
+ * owns both buffers. */
+int qs_steer_rows(float *out, const float *direction, float scale, int n_tokens, int hidden, void *stream);
+
 /* Number of kernels one qs_moe_ffn call with this shape, token count and
  * shared expert (has_shared != 0) launches on the current device: 1 for the
  * persistent decode kernel, 8 for the tensor-core path (which also issues a

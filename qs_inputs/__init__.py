@@ -41,6 +41,8 @@ TAG_SH_GATE = 20
 TAG_SH_UP = 21
 TAG_SH_DOWN = 22
 TAG_SH_SIG = 23
+TAG_DIRECTION = 30
+TAG_ROWS = 31
 
 F32 = 0
 BF16 = 1
@@ -210,3 +212,15 @@ def gen_expert_f32(shape: LayerShape, seed: int, copy: int, e: int):
         return (0.02 * normal(make_key(seed, st, tag, e), 0, rows * cols)).astype(np.float32).reshape(rows, cols)
 
     return draw(TAG_GATE, F, H), draw(TAG_UP, F, H), draw(TAG_DOWN, H, F)
+
+
+def gen_direction(hidden: int, seed: int, copy: int = 0) -> np.ndarray:
+    """A steering direction [hidden] fp32: N(0,1) scaled to unit length (stored normalised)."""
+    z = normal(make_key(seed, stream_of(seed, copy), TAG_DIRECTION), 0, hidden)
+    return (z / np.sqrt(np.sum(z * z))).astype(np.float32)
+
+
+def gen_rows(n: int, hidden: int, seed: int, scale: float = 1.0) -> np.ndarray:
+    """n rows of hidden fp32 values, N(0, scale^2): stand-ins for a layer's output rows."""
+    z = normal(make_key(seed, 0, TAG_ROWS), 0, n * hidden).reshape(n, hidden)
+    return (scale * z).astype(np.float32)

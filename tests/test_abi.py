@@ -82,3 +82,18 @@ def test_invalid_arguments_are_rejected_before_any_launch():
     assert L.qs_workspace_init(fake + 8, 1024, None) == WS
     assert L.qs_test_wait_timeout(fake, 1024, 0, None) == INV
     assert L.qs_read_device_status(None, None) == WS
+
+
+def test_steering_arguments_are_checked_before_any_launch():
+    L = qm.load()
+    fake = 1 << 40
+    INV = qm.QS_ERR_INVALID
+    assert L.qs_steer_rows(None, fake, 1.0, 1, 2048, None) == INV
+    assert L.qs_steer_rows(fake, None, 1.0, 1, 2048, None) == INV
+    assert L.qs_steer_rows(fake, fake, 1.0, 0, 2048, None) == INV
+    assert L.qs_steer_rows(fake, fake, 1.0, 1, 2046, None) == INV   # hidden not a multiple of 4
+    assert L.qs_steer_rows(fake, fake, 1.0, 1, 0, None) == INV
+    assert L.qs_steer_rows(fake + 4, fake, 1.0, 1, 2048, None) == INV
+    assert L.qs_steer_rows(fake, fake + 8, 1.0, 1, 2048, None) == INV
+    # scale 0 is the unsteered path: accepted, and nothing is launched (no device here)
+    assert L.qs_steer_rows(fake, fake, 0.0, 1, 2048, None) == qm.QS_OK
