@@ -26,6 +26,10 @@ _lib = None
 X_F32 = 0
 X_BF16 = 1
 
+# expert weight formats of qs_oracle.c
+FMT = {"q2k": 0, "q4k": 1}
+BLOCK_BYTES = {"q2k": 84, "q4k": 144}
+
 
 def build(force: bool = False) -> str:
     """Compile qs_oracle.c into a shared object (idempotent)."""
@@ -67,6 +71,14 @@ def lib():
             L.qso_moe_ffn.argtypes = [i32, i32, i32, i32, i32, i32, i32, P, i32, P, P, P, i64,
                                       P, P, P, P, P, P, P, P, P, P, P]
             L.qso_steer_rows.argtypes = [i32, i32, P, ctypes.c_double, P]
+            L.qso_q4k_unpack.argtypes = [P, P, P, P, P, P]
+            L.qso_q4k_pack.argtypes = [P, P, P, ctypes.c_uint16, ctypes.c_uint16, P]
+            L.qso_q4k_dequant_rows.argtypes = [P, i64, i64, P]
+            L.qso_q4k_quantize_rows.argtypes = [P, i64, i64, P]
+            L.qso_expert_gateup_fmt.argtypes = [i32, i32, i32, P, P, P]
+            L.qso_expert_down_fmt.argtypes = [i32, i32, i32, P, P, P]
+            L.qso_moe_ffn_fmt.restype = i32
+            L.qso_moe_ffn_fmt.argtypes = [i32] + L.qso_moe_ffn.argtypes
             _lib = L
     return _lib
 
@@ -134,10 +146,48 @@ def q2k_quantize(w: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_expert(gate, up, down) -> np.ndarray:
-    """One expert's Q2_K blob: gate rows, up rows, down rows, concatenated."""
-    return np.concatenate([q2k_quantize(gate).reshape(-1), q2k_quantize(up).reshape(-1),
-                           q2k_quantize(down).reshape(-1)])
+def q4k_unpack(block: np.ndarray):
+    """144 bytes -> (sc[8] u8, m[8] u8, q[256] u8, d bits, dmin bits)."""
+    b = _c(block, np.uint8)
+    assert b.size == 144
+    sc = np.zeros(8, np.uint8)
+    m = np.zeros(8, np.uint8)
+    q = np.zeros(256, np.uint8)
+    d = np.zeros(1, np.uint16)
+    dm = np.zeros(1, np.uint16)
+    lib().qso_q4k_unpack(_p(b), _p(sc), _p(m), _p(q), _p(d), _p(dm))
+    return sc, m, q, int(d[0]), int(dm[0])
+
+
+def q4k_pack(sc, m, q, d: int, dmin: int) -> np.ndarray:
+    out = np.zeros(144, np.uint8)
+    lib().qso_q4k_pack(_p(_c(sc, np.uint8)), _p(_c(m, np.uint8)), _p(_c(q, np.uint8)), d, dmin, _p(out))
+    return out
+
+
+def q4k_dequant(rows: np.ndarray, n_rows: int, K: int) -> np.ndarray:
+    """Q4_K bytes of n_rows rows of K weights -> float64 [n_rows, K] (exact)."""
+    b = _c(rows, np.uint8).reshape(-1)
+    assert b.size >= n_rows * K // 256 * 144
+    w = np.zeros((n_rows, K), np.float64)
+    lib().qso_q4k_dequant_rows(_p(b), n_rows, K, _p(w))
+    return w
+
+
+def q4k_quantize(w: np.ndarray) -> np.ndarray:
+    """fp32 [rows, K] -> Q4_K bytes [rows, K/256*144] (round-to-nearest encoder)."""
+    a = _c(w, np.float32)
+    rows, K = a.shape
+    assert K % 256 == 0
+    out = np.zeros((rows, K // 256 * 144), np.uint8)
+    lib().qso_q4k_quantize_rows(_p(a), rows, K, _p(out))
+    return out
+
+
+def quantize_expert(gate, up, down, fmt: str = "q2k") -> np.ndarray:
+    """One expert's blob in format fmt ("q2k" or "q4k"): gate rows, up rows, down rows, concatenated."""
+    qz = q4k_quantize if fmt == "q4k" else q2k_quantize
+    return np.concatenate([qz(gate).reshape(-1), qz(up).reshape(-1), qz(down).reshape(-1)])
 
 
 # ------------------------------------------------------------------ the layer
@@ -191,7 +241,7 @@ def shared_expert(H, S, sh, xw):
     return hs, float(g[0]), y
 
 
-def moe_ffn(shape, x, Wr, bias, experts, expert_stride, shared, tokens=None, threads=1):
+def moe_ffn(shape, x, Wr, bias, experts, expert_stride, shared, tokens=None, threads=1, fmt="q2k"):
     """The whole layer in double precision.
 
     shape: qs_inputs.LayerShape; x: [T,H] fp32 or bf16 bits; experts: uint8 blob
@@ -226,7 +276,7 @@ def moe_ffn(shape, x, Wr, bias, experts, expert_stride, shared, tokens=None, thr
 
     def run(ts):
         for t in ts:
-            rc = L.qso_moe_ffn(H, E, k, F, S, t, 1, _p(xa), xd, _p(Wr), _p(b), _p(ex), expert_stride,
+            rc = L.qso_moe_ffn_fmt(FMT[fmt], H, E, k, F, S, t, 1, _p(xa), xd, _p(Wr), _p(b), _p(ex), expert_stride,
                                _p(sg), _p(su), _p(sd), _p(ss), _p(ids), _p(p), _p(margin), _p(y),
                                _p(h), _p(hs), _p(gate))
             if rc:

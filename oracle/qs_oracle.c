@@ -198,6 +198,130 @@ void qso_q2k_quantize_rows(const float *w, int64_t n_rows, int64_t K, uint8_t *o
 }
 
 /* ------------------------------------------------------------------ */
+/* Q4_K block (the 4-bit sibling format: routed experts of late layers)  */
+/* ------------------------------------------------------------------ */
+
+/* The pages name Q4_K experts (QuarkStar (q36) README, "Model Weights", the
+ * Layers34-39Q4KExperts file) and say GGUF quant layouts are kept
+ * ("Acknowledgements"); they do not spell the block out.  Reading, the GGUF
+ * Q4_K layout, 144 bytes per 256 weights:
+ *   d (fp16 LE, bytes 0-1) | dmin (fp16 LE, bytes 2-3) | scales[12] (bytes
+ *   4-15) | qs[128] (bytes 16-143);
+ *   eight 32-weight sub-blocks, each with a 6-bit scale sc and a 6-bit min m:
+ *     j < 4:  sc = S[j] & 63,                          m = S[j+4] & 63
+ *     j >= 4: sc = (S[j+4] & 15) | (S[j-4] >> 6) << 4, m = (S[j+4] >> 4) | (S[j] >> 6) << 4
+ *   weight 64c + l (c in 0..3): l < 32 is the low nibble of qs[32c + l]
+ *   (sub-block 2c), l >= 32 the high nibble of qs[32c + l - 32] (sub-block 2c+1);
+ *   w = d * sc * q - dmin * m. */
+#define QSO_Q4K_BYTES 144
+
+void qso_q4k_unpack(const uint8_t *blk, uint8_t *sc, uint8_t *m, uint8_t *q, uint16_t *d, uint16_t *dmin) {
+    const uint8_t *S = blk + 4;
+    for (int j = 0; j < 8; j++) {
+        if (j < 4) {
+            sc[j] = (uint8_t)(S[j] & 63);
+            m[j] = (uint8_t)(S[j + 4] & 63);
+        } else {
+            sc[j] = (uint8_t)((S[j + 4] & 15) | ((S[j - 4] >> 6) << 4));
+            m[j] = (uint8_t)((S[j + 4] >> 4) | ((S[j] >> 6) << 4));
+        }
+    }
+    for (int i = 0; i < QSO_BLOCK_WEIGHTS; i++) {
+        int c = i / 64, l = i % 64;
+        q[i] = (uint8_t)(l < 32 ? (blk[16 + 32 * c + l] & 15) : (blk[16 + 32 * c + l - 32] >> 4));
+    }
+    *d = (uint16_t)(blk[0] | (blk[1] << 8));
+    *dmin = (uint16_t)(blk[2] | (blk[3] << 8));
+}
+
+/* Inverse of qso_q4k_unpack (sc, m in 0..63, q in 0..15). */
+void qso_q4k_pack(const uint8_t *sc, const uint8_t *m, const uint8_t *q, uint16_t d, uint16_t dmin, uint8_t *blk) {
+    memset(blk, 0, QSO_Q4K_BYTES);
+    blk[0] = (uint8_t)(d & 0xff);
+    blk[1] = (uint8_t)(d >> 8);
+    blk[2] = (uint8_t)(dmin & 0xff);
+    blk[3] = (uint8_t)(dmin >> 8);
+    uint8_t *S = blk + 4;
+    for (int j = 0; j < 4; j++) {
+        S[j] = (uint8_t)((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        S[j + 4] = (uint8_t)((m[j] & 63) | ((m[j + 4] >> 4) << 6));
+        S[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+    }
+    for (int i = 0; i < QSO_BLOCK_WEIGHTS; i++) {
+        int c = i / 64, l = i % 64;
+        if (l < 32) blk[16 + 32 * c + l] |= (uint8_t)(q[i] & 15);
+        else blk[16 + 32 * c + l - 32] |= (uint8_t)((q[i] & 15) << 4);
+    }
+}
+
+/* Decode one row of K weights (K/256 consecutive Q4_K blocks) to double, exactly. */
+void qso_q4k_dequant_row(const uint8_t *row, int64_t K, double *w) {
+    uint8_t sc[8], m[8], q[256];
+    uint16_t dh, mh;
+    for (int64_t b = 0; b < K / QSO_BLOCK_WEIGHTS; b++) {
+        qso_q4k_unpack(row + b * QSO_Q4K_BYTES, sc, m, q, &dh, &mh);
+        double d = qso_half_to_double(dh), dmin = qso_half_to_double(mh);
+        for (int i = 0; i < QSO_BLOCK_WEIGHTS; i++) {
+            int j = i / 32;
+            w[b * QSO_BLOCK_WEIGHTS + i] = d * (double)sc[j] * (double)q[i] - dmin * (double)m[j];
+        }
+    }
+}
+
+void qso_q4k_dequant_rows(const uint8_t *rows, int64_t n_rows, int64_t K, double *w) {
+    int64_t row_bytes = K / QSO_BLOCK_WEIGHTS * QSO_Q4K_BYTES;
+    for (int64_t r = 0; r < n_rows; r++) qso_q4k_dequant_row(rows + r * row_bytes, K, w + r * K);
+}
+
+/* Round-to-nearest Q4_K encoder (set-up step, not part of the layer), the same
+ * reading as the Q2_K one with 32-weight sub-blocks, 4-bit codes and 6-bit
+ * scales: per sub-block m = max(0, -min w), s = (max w + m)/15; per block
+ * d = fp16(max s / 63), dmin = fp16(max m / 63); sc = clamp(rint(s/d),0,63),
+ * mc = clamp(rint(m/dmin),0,63) (0 when the divisor is 0);
+ * q = clamp(rint((w + dmin*mc)/(d*sc)),0,15), 0 when d*sc is 0.  All in fp32,
+ * one rounding per operation, ties to even. */
+void qso_q4k_quantize_rows(const float *w, int64_t n_rows, int64_t K, uint8_t *out) {
+    int64_t nb = K / QSO_BLOCK_WEIGHTS;
+    for (int64_t r = 0; r < n_rows; r++) {
+        for (int64_t b = 0; b < nb; b++) {
+            const float *x = w + r * K + b * QSO_BLOCK_WEIGHTS;
+            float s[8], mm[8], maxs = 0.0f, maxm = 0.0f;
+            for (int j = 0; j < 8; j++) {
+                float mn = x[32 * j], mx = x[32 * j];
+                for (int i = 1; i < 32; i++) {
+                    float v = x[32 * j + i];
+                    if (v < mn) mn = v;
+                    if (v > mx) mx = v;
+                }
+                mm[j] = mn < 0.0f ? -mn : 0.0f;
+                s[j] = (mx + mm[j]) / 15.0f;
+                if (s[j] > maxs) maxs = s[j];
+                if (mm[j] > maxm) maxm = mm[j];
+            }
+            uint16_t dh = qso_float_to_half(maxs / 63.0f);
+            uint16_t mh = qso_float_to_half(maxm / 63.0f);
+            float df = (float)qso_half_to_double(dh);
+            float mf = (float)qso_half_to_double(mh);
+            uint8_t sc[8], mc[8], q[256];
+            for (int j = 0; j < 8; j++) {
+                int a = df > 0.0f ? (int)clampf_(rintf(s[j] / df), 0.0f, 63.0f) : 0;
+                int c = mf > 0.0f ? (int)clampf_(rintf(mm[j] / mf), 0.0f, 63.0f) : 0;
+                sc[j] = (uint8_t)a;
+                mc[j] = (uint8_t)c;
+                float step = df * (float)a;
+                float base = mf * (float)c;
+                for (int i = 0; i < 32; i++) {
+                    int qi = 0;
+                    if (step > 0.0f) qi = (int)clampf_(rintf((x[32 * j + i] + base) / step), 0.0f, 15.0f);
+                    q[32 * j + i] = (uint8_t)qi;
+                }
+            }
+            qso_q4k_pack(sc, mc, q, dh, mh, out + (r * nb + b) * QSO_Q4K_BYTES);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* the layer                                                            */
 /* ------------------------------------------------------------------ */
 
@@ -268,36 +392,57 @@ void qso_group(int E, int k, int T, const int32_t *ids, int32_t *counts, int32_t
             if (ids[i] == e) perm[pos++] = (int32_t)i;
 }
 
+/* Expert weight formats: fmt 0 = Q2_K (84-byte blocks), 1 = Q4_K (144-byte blocks). */
+#define QSO_FMT_Q2K 0
+#define QSO_FMT_Q4K 1
+
+static int64_t row_bytes_(int fmt, int64_t K) {
+    return K / QSO_BLOCK_WEIGHTS * (fmt == QSO_FMT_Q4K ? QSO_Q4K_BYTES : QSO_BLOCK_BYTES);
+}
+
+static void dequant_row_(int fmt, const uint8_t *row, int64_t K, double *w) {
+    if (fmt == QSO_FMT_Q4K) qso_q4k_dequant_row(row, K, w);
+    else qso_q2k_dequant_row(row, K, w);
+}
+
 /* One routed expert on one widened token: h = silu(Wg x) * (Wu x).
- * blob = the expert's Q2_K bytes: gate rows [F x H], then up rows [F x H],
- * then down rows [H x F]; blocks run along each row. */
-void qso_expert_gateup(int H, int F, const uint8_t *blob, const double *x, double *h) {
-    int64_t rb = (int64_t)H / QSO_BLOCK_WEIGHTS * QSO_BLOCK_BYTES;
+ * blob = the expert's bytes in format fmt: gate rows [F x H], then up rows
+ * [F x H], then down rows [H x F]; blocks run along each row. */
+void qso_expert_gateup_fmt(int fmt, int H, int F, const uint8_t *blob, const double *x, double *h) {
+    int64_t rb = row_bytes_(fmt, H);
     double *w = (double *)malloc(sizeof(double) * (size_t)H);
     for (int r = 0; r < F; r++) {
         double g = 0.0, u = 0.0;
-        qso_q2k_dequant_row(blob + (int64_t)r * rb, H, w);
+        dequant_row_(fmt, blob + (int64_t)r * rb, H, w);
         for (int i = 0; i < H; i++) g += w[i] * x[i];
-        qso_q2k_dequant_row(blob + (int64_t)(F + r) * rb, H, w);
+        dequant_row_(fmt, blob + (int64_t)(F + r) * rb, H, w);
         for (int i = 0; i < H; i++) u += w[i] * x[i];
         h[r] = silu_(g) * u;
     }
     free(w);
 }
 
+void qso_expert_gateup(int H, int F, const uint8_t *blob, const double *x, double *h) {
+    qso_expert_gateup_fmt(QSO_FMT_Q2K, H, F, blob, x, h);
+}
+
 /* y = Wd h for one expert (down rows [H x F] after gate and up). */
-void qso_expert_down(int H, int F, const uint8_t *blob, const double *h, double *y) {
-    int64_t rb_h = (int64_t)H / QSO_BLOCK_WEIGHTS * QSO_BLOCK_BYTES;
-    int64_t rb_f = (int64_t)F / QSO_BLOCK_WEIGHTS * QSO_BLOCK_BYTES;
+void qso_expert_down_fmt(int fmt, int H, int F, const uint8_t *blob, const double *h, double *y) {
+    int64_t rb_h = row_bytes_(fmt, H);
+    int64_t rb_f = row_bytes_(fmt, F);
     const uint8_t *down = blob + 2 * (int64_t)F * rb_h;
     double *w = (double *)malloc(sizeof(double) * (size_t)F);
     for (int r = 0; r < H; r++) {
         double acc = 0.0;
-        qso_q2k_dequant_row(down + (int64_t)r * rb_f, F, w);
+        dequant_row_(fmt, down + (int64_t)r * rb_f, F, w);
         for (int i = 0; i < F; i++) acc += w[i] * h[i];
         y[r] = acc;
     }
     free(w);
+}
+
+void qso_expert_down(int H, int F, const uint8_t *blob, const double *h, double *y) {
+    qso_expert_down_fmt(QSO_FMT_Q2K, H, F, blob, h, y);
 }
 
 /* Gated bf16 shared expert on one widened token:
@@ -327,11 +472,11 @@ void qso_shared_expert(int H, int S, const uint16_t *wg, const uint16_t *wu, con
  *   ids [T x k], p [T x k], margin [T], y [T x H]   (required)
  *   h [T*k x F] (SwiGLU of each (t, slot)), hs [T x S], gate [T]  (nullable)
  * S == 0 or wg == NULL skips the shared expert. */
-int qso_moe_ffn(int H, int E, int k, int F, int S, int t0, int nt, const void *x, int x_dtype,
-                const float *Wr, const float *bias, const uint8_t *experts, int64_t expert_stride,
-                const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, const uint16_t *wsig,
-                int32_t *ids, double *p, double *margin, double *y, double *h_out, double *hs_out,
-                double *gate_out) {
+int qso_moe_ffn_fmt(int fmt, int H, int E, int k, int F, int S, int t0, int nt, const void *x, int x_dtype,
+                    const float *Wr, const float *bias, const uint8_t *experts, int64_t expert_stride,
+                    const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, const uint16_t *wsig,
+                    int32_t *ids, double *p, double *margin, double *y, double *h_out, double *hs_out,
+                    double *gate_out) {
     size_t xb = (size_t)H * (x_dtype == QSO_X_BF16 ? 2 : 4);
     double *xw = (double *)malloc(sizeof(double) * (size_t)H);
     double *h = (double *)malloc(sizeof(double) * (size_t)F);
@@ -349,9 +494,9 @@ int qso_moe_ffn(int H, int E, int k, int F, int S, int t0, int nt, const void *x
         for (int j = 0; j < k; j++) {
             int e = ids[(size_t)t * k + j];
             const uint8_t *blob = experts + (int64_t)e * expert_stride;
-            qso_expert_gateup(H, F, blob, xw, h);
+            qso_expert_gateup_fmt(fmt, H, F, blob, xw, h);
             if (h_out) memcpy(h_out + ((size_t)t * k + j) * F, h, sizeof(double) * (size_t)F);
-            qso_expert_down(H, F, blob, h, ye);
+            qso_expert_down_fmt(fmt, H, F, blob, h, ye);
             for (int i = 0; i < H; i++) yt[i] += p[(size_t)t * k + j] * ye[i];
         }
         if (S > 0 && wg) {
@@ -364,6 +509,16 @@ int qso_moe_ffn(int H, int E, int k, int F, int S, int t0, int nt, const void *x
     }
     free(xw); free(h); free(ye); free(hs);
     return rc;
+}
+
+/* The layer with Q2_K experts (see qso_moe_ffn_fmt). */
+int qso_moe_ffn(int H, int E, int k, int F, int S, int t0, int nt, const void *x, int x_dtype,
+                const float *Wr, const float *bias, const uint8_t *experts, int64_t expert_stride,
+                const uint16_t *wg, const uint16_t *wu, const uint16_t *wd, const uint16_t *wsig,
+                int32_t *ids, double *p, double *margin, double *y, double *h_out, double *hs_out,
+                double *gate_out) {
+    return qso_moe_ffn_fmt(QSO_FMT_Q2K, H, E, k, F, S, t0, nt, x, x_dtype, Wr, bias, experts, expert_stride, wg, wu,
+                           wd, wsig, ids, p, margin, y, h_out, hs_out, gate_out);
 }
 
 /* ------------------------------------------------------------------ */
