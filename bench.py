@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--max-copies", type=int, default=48)
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--format", default="q2k", choices=["q2k", "q4k"],
+                    help="routed expert format: Q2_K (the workloads' format) or Q4_K (per-step kernels)")
     ap.add_argument("--steer", type=float, default=0.0,
                     help="directional steering of every output row with this scale (0: off)")
     return ap.parse_args()
@@ -176,7 +178,12 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ the oracle on host cores
 
-def oracle_sample_layer(w, T, n_tokens, copy=0):
+def expert_bytes(sh, fmt="q2k"):
+    """Bytes of one routed expert (gate, up, down) in Q2_K (84 B) or Q4_K (144 B) blocks of 256 weights."""
+    return (144 if fmt == "q4k" else 84) * 3 * sh.expert_ffn * sh.hidden // 256
+
+
+def oracle_sample_layer(w, T, n_tokens, copy=0, fmt="q2k"):
     """Host layer for the oracle: x pool tokens 0..n_tokens-1, experts those tokens route to."""
     import oracle
     import concurrent.futures as cf
@@ -186,28 +193,28 @@ def oracle_sample_layer(w, T, n_tokens, copy=0):
     bias = qi.gen_bias(sh, w.seed, copy, w.zipf_bias)
     shared = qi.gen_shared(sh, w.seed, copy)
     ids, _, _, _ = oracle.route(xb, oracle.X_BF16 if sh.x_dtype == qi.BF16 else oracle.X_F32, Wr, bias, sh.top_k)
-    blob = np.zeros(sh.n_experts * sh.expert_bytes, np.uint8)
+    eb = expert_bytes(sh, fmt)
+    blob = np.zeros(sh.n_experts * eb, np.uint8)
 
     def one(e):
-        blob[e * sh.expert_bytes:(e + 1) * sh.expert_bytes] = oracle.quantize_expert(
-            *qi.gen_expert_f32(sh, w.seed, copy, int(e)))
+        blob[e * eb:(e + 1) * eb] = oracle.quantize_expert(*qi.gen_expert_f32(sh, w.seed, copy, int(e)), fmt=fmt)
 
     with cf.ThreadPoolExecutor(max(1, min(16, os.cpu_count() or 1))) as ex:
         list(ex.map(one, np.unique(ids)))
     return xb, Wr, bias, shared, blob
 
 
-def time_oracle(w, T, budget_s, max_calls=None):
+def time_oracle(w, T, budget_s, max_calls=None, fmt="q2k"):
     """Run the oracle, one layer call of T tokens at a time on one core, for ~budget_s seconds."""
     import oracle
     T = min(T, ORACLE_TOKENS_MAX)
     n_pool = 16 if T == 1 else max(T, 16)
-    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
+    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool, fmt=fmt)
     calls, tokens = 0, 0
     t0 = time.perf_counter()
     while True:
         t_start = (calls * T) % max(1, n_pool - T + 1)
-        oracle.moe_ffn(w.shape, xb[t_start:t_start + T], Wr, bias, blob, w.shape.expert_bytes, shared)
+        oracle.moe_ffn(w.shape, xb[t_start:t_start + T], Wr, bias, blob, expert_bytes(w.shape, fmt), shared, fmt=fmt)
         calls += 1
         tokens += T
         el = time.perf_counter() - t0
@@ -238,11 +245,12 @@ def run_reference(args, w, T):
     T_full = T
     T = min(T, ORACLE_TOKENS_MAX)
     n_pool = max(T, 16)
-    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool)
+    xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool, fmt=args.format)
 
     def step(i):
         t0 = (i * T) % max(1, n_pool - T + 1)
-        oracle.moe_ffn(w.shape, xb[t0:t0 + T], Wr, bias, blob, w.shape.expert_bytes, shared)
+        oracle.moe_ffn(w.shape, xb[t0:t0 + T], Wr, bias, blob, expert_bytes(w.shape, args.format), shared,
+                       fmt=args.format)
 
     for i in range(args.warmup):
         step(i)
@@ -253,7 +261,8 @@ def run_reference(args, w, T):
     ms = el / args.steps * 1e3
     val = T * args.steps / el
     line = {
-        "impl": "reference", "metric": metric_name(T_full), "value": val,
+        "impl": "reference", "metric": metric_name(T_full) + (" [Q4_K experts]" if args.format == "q4k" else ""),
+        "value": val,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
@@ -288,7 +297,9 @@ def config_of(w, T, args):
     s = w.shape
     return {"workload": w.name, "hidden": s.hidden, "n_experts": s.n_experts, "top_k": s.top_k,
             "expert_ffn": s.expert_ffn, "shared_ffn": s.shared_ffn, "n_tokens": T, "layer_copies": w.copies,
-            "x_pool": qi.X_POOL, "expert_format": "Q2_K (84 B / 256 weights)", "zipf_bias": w.zipf_bias,
+            "x_pool": qi.X_POOL, "zipf_bias": w.zipf_bias,
+            "expert_format": "Q4_K (144 B / 256 weights)" if getattr(args, "format", "q2k") == "q4k"
+            else "Q2_K (84 B / 256 weights)",
             "layer_copies_cycled": getattr(args, "copies_used", w.copies),
             "l2": ("inputs larger than L2: %d layer copies cycled, no flush" % getattr(args, "copies_used", w.copies))
                   if args.l2 == "cycle" else
@@ -299,12 +310,13 @@ def config_of(w, T, args):
 
 # ------------------------------------------------------------------ our arm
 
-def device_layers(w, qm, torch, device, copies):
+def device_layers(w, qm, torch, device, copies, fmt="q2k"):
     """Layer copies resident in HBM, drawn on the device (experts quantised by the library's encoder)."""
     sh = w.shape
     H, E, k, F, S = sh.hidden, sh.n_experts, sh.top_k, sh.expert_ffn, sh.shared_ffn
-    stride = sh.expert_bytes
-    gbytes = F * H // 256 * 84
+    stride = expert_bytes(sh, fmt)
+    gbytes = F * H // 256 * (144 if fmt == "q4k" else 84)
+    quantize = qm.qs_q4k_quantize if fmt == "q4k" else qm.qs_q2k_quantize
     layers = []
     for c in range(copies):
         gen = torch.Generator(device=device)
@@ -317,23 +329,24 @@ def device_layers(w, qm, torch, device, copies):
                 wts = torch.randn((n, rows, cols), generator=gen, device=device, dtype=torch.float32) * 0.02
                 for i in range(n):
                     base = blob.data_ptr() + (e0 + i) * stride + off
-                    qm.qs_q2k_quantize(wts[i], base)
+                    quantize(wts[i], base)
         Wr = torch.randn((E, H), generator=gen, device=device, dtype=torch.float32) * 0.02
         b = qi.gen_bias(sh, w.seed, c, w.zipf_bias)
         bias = None if b is None else torch.from_numpy(b).to(device)
         shd = {n_: (torch.randn(shp, generator=gen, device=device, dtype=torch.float32) * 0.02).to(torch.bfloat16)
                for n_, shp in (("gate", (S, H)), ("up", (S, H)), ("down", (H, S)), ("sig", (H,)))}
-        layers.append({"blob": blob, "experts": qm.make_experts(blob, stride), "Wr": Wr, "bias": bias, "sh": shd,
+        make = qm.make_q4k_experts if fmt == "q4k" else qm.make_experts
+        layers.append({"blob": blob, "experts": make(blob, stride), "Wr": Wr, "bias": bias, "sh": shd,
                        "shared": qm.make_shared(shd["gate"], shd["up"], shd["down"], shd["sig"])})
     torch.cuda.synchronize()
     return layers
 
 
-def algorithmic_bytes(sh, T, distinct):
+def algorithmic_bytes(sh, T, distinct, fmt="q2k"):
     """Bytes the layer must move for one call: router, x, the distinct experts' Q2_K, shared, out."""
     router = sh.n_experts * sh.hidden * 4
     x = T * sh.hidden * (2 if sh.x_dtype == qi.BF16 else 4)
-    experts = distinct * sh.expert_bytes
+    experts = distinct * expert_bytes(sh, fmt)
     shared = (3 * sh.shared_ffn * sh.hidden + sh.hidden) * 2
     out = T * sh.hidden * 4
     return router + x + experts + shared + out, experts
@@ -352,7 +365,8 @@ def run_ours(args, w, T):
     sh = w.shape
     H = sh.hidden
     shape = qm.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.expert_ffn, sh.shared_ffn, sh.x_dtype)
-    launches_per_step = qm.qs_moe_ffn_launches(shape, T, True)
+    launches_per_step = qm.qs_moe_ffn_launches(shape, T, True) if args.format == "q2k" else \
+        (6 if sh.shared_ffn > 0 else 4)   # Q4_K: shared gate/up, route, group, gate/up, down, shared down
     if launches_per_step < 1:
         raise SystemExit(f"qs_moe_ffn_launches failed ({launches_per_step})")
     layer_launches = launches_per_step
@@ -361,15 +375,15 @@ def run_ours(args, w, T):
 
     # copies: the workload's own count, or enough that nothing a step reads is still in L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    per_step_upper = algorithmic_bytes(sh, T, min(sh.n_experts, T * sh.top_k))[0]
+    per_step_upper = algorithmic_bytes(sh, T, min(sh.n_experts, T * sh.top_k), args.format)[0]
     copies = w.copies
     if args.l2 == "cycle":
-        copy_bytes = sh.n_experts * sh.expert_bytes + (3 * sh.shared_ffn * H + H) * 2 + sh.n_experts * H * 4
+        copy_bytes = sh.n_experts * expert_bytes(sh, args.format) + (3 * sh.shared_ffn * H + H) * 2 + sh.n_experts * H * 4
         want = math.ceil(3 * l2 / max(per_step_upper, 1))
         budget = int(0.5 * torch.cuda.get_device_properties(device).total_memory / copy_bytes)
         copies = max(w.copies, min(want, args.max_copies, budget))
     args.copies_used = copies
-    layers = device_layers(w, qm, torch, device, copies)
+    layers = device_layers(w, qm, torch, device, copies, args.format)
 
     # x pool: rows wrap so that rows [j, j+T) are contiguous for every j < X_POOL
     xb, _ = qi.gen_x(sh, w.seed, qi.X_POOL + (T if T > qi.X_POOL else 0))
@@ -387,7 +401,8 @@ def run_ours(args, w, T):
 
     def step(i, x=None, n_layers=None):
         Ld = layers[i % (n_layers or len(layers))]
-        qm.qs_moe_ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T,
+        ffn = qm.qs_moe_ffn_q4k if args.format == "q4k" else qm.qs_moe_ffn
+        ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T,
                       ws, stream)
         if args.steer:
             qm.qs_steer_rows(out, direction, args.steer, T, stream)
@@ -496,7 +511,7 @@ def run_ours(args, w, T):
                  "note": "qs_steer_rows alone, K back-to-back calls on the layer's output rows (L2-resident)"}
 
     # roofline of the layer kernel: algorithmic bytes over the measured step time
-    algo = [algorithmic_bytes(sh, T, distinct[(args.warmup + j) % period]) for j in range(K)]
+    algo = [algorithmic_bytes(sh, T, distinct[(args.warmup + j) % period], args.format) for j in range(K)]
     algo_bytes = float(np.mean([a for a, _ in algo])) + (H * 4 if args.steer else 0)
     q2k_bytes = float(np.mean([q for _, q in algo]))
     mean_step_s = total_s / K
@@ -509,13 +524,13 @@ def run_ours(args, w, T):
         return
     cpu = None
     if not args.no_cpu_baseline and dist.world == 1:
-        rate, calls, el = time_oracle(w, T, args.cpu_seconds)
+        rate, calls, el = time_oracle(w, T, args.cpu_seconds, fmt=args.format)
         ts = min(T, ORACLE_TOKENS_MAX)
         cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{calls} layer calls of {ts} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
                          f"the experts they route to" + (" (per-token cost independent of the batch)" if T > ts else "")
                          + f"; {cpu_model()}"}
-    if layer_launches > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
+    if args.format == "q2k" and layer_launches > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
         flops = layer_flops(sh, T)
         tf_peak = pk["bf16_tflops"] if pk else 1900.0
         tf = flops / mean_step_s / 1e12
@@ -526,18 +541,20 @@ def run_ours(args, w, T):
                 "algorithmic_flops_per_launch": flops, "traffic": None}
     else:
         roof = {"bound": "hbm",
-                "kernel": "fused_decode_kernel" if layer_launches == 1 else "qs_moe_ffn (whole layer)",
+                "kernel": ("fused_decode_kernel" if layer_launches == 1 else "qs_moe_ffn (whole layer)")
+                if args.format == "q2k" else "qs_moe_ffn_q4k (whole layer, %d kernels)" % layer_launches,
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
                 "algorithmic_bytes_per_launch": algo_bytes,
                 "traffic": recorded_traffic(w.name) if layer_launches == 1 and T == w.tokens[0] and not args.steer
                 else None}
     line = {
-        "metric": metric_name(T),
+        "metric": metric_name(T) + (" [Q4_K experts]" if args.format == "q4k" else ""),
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step_s * 1e3, "us_per_layer": mean_step_s * 1e6,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "q2k-int16dot-f32" if roof["bound"] == "hbm" else "q2k-dequant-f16-mma-f32", "data": "synthetic",
+        "dtype": ("q4k-f32" if args.format == "q4k" else
+                  "q2k-int16dot-f32" if roof["bound"] == "hbm" else "q2k-dequant-f16-mma-f32"), "data": "synthetic",
         "config": config_of(w, T, args),
         "achieved_gbs_all_bytes": achieved, "achieved_gbs_q2k_bytes": q2k_bytes / mean_step_s / 1e9,
         "roofline": roof,

@@ -260,6 +260,58 @@ int qs_q2k_quantize(const float* w, int64_t n_rows, int64_t K, void* out, void* 
     return e == cudaSuccess ? QS_OK : cuda_fail(e);
 }
 
+int qs_moe_ffn_q4k(const qs_moe_shape* shape, const void* x, const float* router_w, const float* router_bias,
+                   const qs_q4k_experts* experts, const qs_shared_expert* shared, float* out, int n_tokens,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+    if (!shape_ok(shape) || !x || !router_w || !out || n_tokens < 1) return QS_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(router_w)) return QS_ERR_INVALID;
+    if (!experts || !experts->blocks || !aligned16(experts->blocks)) return QS_ERR_INVALID;
+    const int64_t need = 144ll * 3ll * shape->expert_ffn * shape->hidden / 256;
+    if (experts->expert_stride < need || experts->expert_stride % 16) return QS_ERR_INVALID;
+    const bool has_shared = shape->shared_ffn > 0 && shared != nullptr;
+    if (has_shared && !shared_ok(shape, shared)) return QS_ERR_INVALID;
+    if (q4k_down_smem(shape->top_k, shape->expert_ffn) > 200 * 1024) return QS_ERR_UNSUPPORTED;
+    if (int rc = check_ws(shape, n_tokens, workspace, workspace_bytes)) return rc;
+    const WsLayout L = ws_layout(*shape, n_tokens);
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint8_t* blocks = static_cast<const uint8_t*>(experts->blocks);
+    float* hs = ws_at<float>(workspace, L.hs);
+    float* gate = ws_at<float>(workspace, L.gate);
+    int32_t* ids = ws_at<int32_t>(workspace, L.ids);
+    float* pw = ws_at<float>(workspace, L.pw);
+    cudaError_t e;
+    if (has_shared) {
+        e = launch_shared_gateup(*shape, x, (const uint16_t*)shared->w_gate, (const uint16_t*)shared->w_up,
+                                 (const uint16_t*)shared->w_gate_sig, n_tokens, hs, gate, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_route(*shape, x, router_w, router_bias, n_tokens, ws_at<float>(workspace, L.logits), ids, pw,
+                     ws_at<uint32_t>(workspace, L.tickets), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_group(shape->n_experts, shape->top_k, n_tokens, ids, ws_at<int32_t>(workspace, L.counts),
+                     ws_at<int32_t>(workspace, L.offsets), ws_at<int32_t>(workspace, L.perm), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_q4k_gateup(*shape, x, blocks, experts->expert_stride, ws_at<int32_t>(workspace, L.offsets),
+                          ws_at<int32_t>(workspace, L.perm), n_tokens, ws_at<float>(workspace, L.h), st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = launch_q4k_down(*shape, blocks, experts->expert_stride, ws_at<float>(workspace, L.h), ids, pw, n_tokens, out,
+                        st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (has_shared) {  // + gate * Wsd hs, added onto the routed rows
+        e = launch_down(*shape, nullptr, 0, nullptr, nullptr, nullptr, 0, (const uint16_t*)shared->w_down, hs, gate,
+                        n_tokens, out, 1, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return QS_OK;
+}
+
+int qs_q4k_quantize(const float* w, int64_t n_rows, int64_t K, void* out, void* stream) {
+    if (!w || !out || n_rows < 1 || K < 256 || K % 256 || !aligned16(w) || ((uintptr_t)out & 3u))
+        return QS_ERR_INVALID;
+    cudaError_t e = launch_q4k_quantize(w, n_rows * (K / 256), static_cast<uint8_t*>(out), (cudaStream_t)stream);
+    return e == cudaSuccess ? QS_OK : cuda_fail(e);
+}
+
 int qs_steer_rows(float* out, const float* direction, float scale, int n_tokens, int hidden, void* stream) {
     if (!out || !direction || n_tokens < 1 || hidden < 4 || hidden % 4 || !aligned16(out) || !aligned16(direction))
         return QS_ERR_INVALID;

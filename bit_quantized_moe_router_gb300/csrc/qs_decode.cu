@@ -619,8 +619,14 @@ __global__ void test_wait_kernel(WsHeader* hdr, uint64_t limit_ns) {
 
 static inline size_t align16(size_t v) { return (v + 15) / 16 * 16; }
 
+// Opt a kernel in to `bytes` of dynamic shared memory when its dynamic plus static shared
+// memory passes the 48 KB a launch gets without the attribute.
 static cudaError_t set_smem(const void* fn, size_t bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes == 0) return cudaSuccess;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    if (bytes + fa.sharedSizeBytes <= 48 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 

@@ -57,6 +57,15 @@ cudaError_t launch_shared_gateup(const qs_moe_shape& s, const void* x, const uin
 cudaError_t launch_quantize(const float* w, int64_t n_blocks, uint8_t* out, cudaStream_t st);
 cudaError_t launch_test_wait(void* ws, uint64_t limit_ns, cudaStream_t st);
 
+// Q4_K routed experts (qs_q4k.cu): encoder, gate/up + SwiGLU into h, down + routing-weight
+// combine into out (stored, not added).
+cudaError_t launch_q4k_quantize(const float* w, int64_t n_blocks, uint8_t* out, cudaStream_t st);
+cudaError_t launch_q4k_gateup(const qs_moe_shape& s, const void* x, const uint8_t* experts, int64_t stride,
+                              const int32_t* offsets, const int32_t* perm, int T, float* h, cudaStream_t st);
+cudaError_t launch_q4k_down(const qs_moe_shape& s, const uint8_t* experts, int64_t stride, const float* h,
+                            const int32_t* ids, const float* pw, int T, float* out, cudaStream_t st);
+size_t q4k_down_smem(int k, int F);
+
 // Directional steering of output rows (qs_steer.cu): y <- y - scale * d * (d . y) per row.
 cudaError_t launch_steer_rows(float* y, const float* d, float scale, int T, int H, cudaStream_t st);
 

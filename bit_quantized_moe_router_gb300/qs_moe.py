@@ -22,7 +22,7 @@ EXPORTS = (
     "qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes", "qs_workspace_init",
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
     "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
-    "qs_moe_ffn_noalloc", "qs_steer_rows",
+    "qs_moe_ffn_noalloc", "qs_steer_rows", "qs_moe_ffn_q4k", "qs_q4k_quantize",
 )
 
 
@@ -38,6 +38,10 @@ class qs_moe_shape(ctypes.Structure):
 
 
 class qs_q2k_experts(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_void_p), ("expert_stride", ctypes.c_int64)]
+
+
+class qs_q4k_experts(ctypes.Structure):
     _fields_ = [("blocks", ctypes.c_void_p), ("expert_stride", ctypes.c_int64)]
 
 
@@ -86,6 +90,8 @@ def load(build_if_missing: bool = True):
     L.qs_q2k_quantize.argtypes = [P, i64, i64, P, P]
     L.qs_test_wait_timeout.argtypes = [P, sz, i32, P]
     L.qs_steer_rows.argtypes = [P, P, ctypes.c_float, i32, i32, P]
+    L.qs_moe_ffn_q4k.argtypes = [SP, P, P, P, ctypes.POINTER(qs_q4k_experts), HP, P, i32, P, sz, P]
+    L.qs_q4k_quantize.argtypes = [P, i64, i64, P, P]
     for name in EXPORTS:
         if name not in ("qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes"):
             getattr(L, name).restype = i32
@@ -124,6 +130,10 @@ def make_shape(hidden, n_experts, top_k, expert_ffn, shared_ffn, x_dtype) -> qs_
 
 def make_experts(blocks, expert_stride: int) -> qs_q2k_experts:
     return qs_q2k_experts(_ptr(blocks), expert_stride)
+
+
+def make_q4k_experts(blocks, expert_stride: int) -> qs_q4k_experts:
+    return qs_q4k_experts(_ptr(blocks), expert_stride)
 
 
 def make_shared(w_gate, w_up, w_down, w_gate_sig) -> qs_shared_expert:
@@ -213,6 +223,20 @@ def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:
 def qs_q2k_quantize(w, out, stream=None):
     rows, K = w.shape
     _check(load().qs_q2k_quantize(_ptr(w), rows, K, _ptr(out), _stream(stream)), "qs_q2k_quantize")
+
+
+def qs_q4k_quantize(w, out, stream=None):
+    rows, K = w.shape
+    _check(load().qs_q4k_quantize(_ptr(w), rows, K, _ptr(out), _stream(stream)), "qs_q4k_quantize")
+
+
+def qs_moe_ffn_q4k(shape, x, router_w, router_bias, experts: qs_q4k_experts, shared, out, n_tokens, workspace,
+                   stream=None):
+    """The whole layer with Q4_K routed experts (same arguments as qs_moe_ffn)."""
+    _check(load().qs_moe_ffn_q4k(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
+                                 ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _ptr(out),
+                                 n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _stream(stream)), "qs_moe_ffn_q4k")
 
 
 def qs_test_wait_timeout(workspace, limit_us, stream=None):

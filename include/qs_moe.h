@@ -88,6 +88,17 @@ typedef struct {
     int64_t expert_stride;  /* bytes between experts, >= the expert's Q2_K bytes, % 16 == 0 */
 } qs_q2k_experts;
 
+/* Routed experts in Q4_K (device memory, read only): per expert gate rows
+ * [F x H], up rows [F x H], down rows [H x F], 144-byte blocks of 256 weights
+ * along each row (GGUF Q4_K layout, which the pages keep: QuarkStar (q36)
+ * README, "Acknowledgements"; Q4_K experts: its "Model Weights" section):
+ * d (fp16 LE) | dmin (fp16 LE) | 12 bytes of 6-bit scales and mins for eight
+ * 32-weight sub-blocks | 128 bytes of 4-bit codes. */
+typedef struct {
+    const void *blocks;     /* expert 0's first byte; 16-byte aligned             */
+    int64_t expert_stride;  /* bytes between experts, >= the expert's Q4_K bytes, % 16 == 0 */
+} qs_q4k_experts;
+
 /* bf16 shared expert (device memory, read only, row-major). */
 typedef struct {
     const void *w_gate;      /* [S x H] */
@@ -204,6 +215,25 @@ int qs_moe_ffn(const qs_moe_shape *shape, const void *x, const float *router_w, 
 int qs_moe_ffn_noalloc(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
                        const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                        void *stream);
+
+/* The whole layer with Q4_K routed experts: the same routing, grouping and
+ * gated bf16 shared expert as qs_moe_ffn, the routed gate/up (SwiGLU) and down
+ * projections dequantising Q4_K blocks (w = d*sc*q - dmin*m per 32-weight
+ * sub-block) against fp32 activations with fp32 accumulation.  Arguments,
+ * layouts, workspace (qs_moe_workspace_bytes of the same shape) and error
+ * behaviour as qs_moe_ffn; expert_stride must cover 144*3*F*H/256 bytes.
+ * Runs the per-step kernels: up to six launches on `stream`. */
+int qs_moe_ffn_q4k(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
+                   const qs_q4k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Q4_K encoder (weight set-up, not part of the layer): round-to-nearest, per
+ * 32-weight sub-block m = max(0, -min), s = (max + m)/15, per block
+ * d = fp16(max s / 63), dmin = fp16(max m / 63), 6-bit scale and min codes and
+ * 4-bit weight codes by rint, every decision in fp32.  w device fp32
+ * [n_rows x K], K % 256 == 0, 16-byte aligned; out device [n_rows x K/256 x
+ * 144] bytes (4-byte aligned). */
+int qs_q4k_quantize(const float *w, int64_t n_rows, int64_t K, void *out, void *stream);
 
 /* Directional steering of the layer's output, in place (QuarkStar (q36)
  * README, "Steering"; DwarfStar (ds4) page, "Steering"): every token row

@@ -97,3 +97,25 @@ def test_steering_arguments_are_checked_before_any_launch():
     assert L.qs_steer_rows(fake, fake + 8, 1.0, 1, 2048, None) == INV
     # scale 0 is the unsteered path: accepted, and nothing is launched (no device here)
     assert L.qs_steer_rows(fake, fake, 0.0, 1, 2048, None) == qm.QS_OK
+
+
+def test_q4k_arguments_are_checked_before_any_launch():
+    L = qm.load()
+    fake = 1 << 40
+    B = ctypes.byref
+    INV, WS = qm.QS_ERR_INVALID, qm.QS_ERR_WORKSPACE
+    shape = qm.make_shape(2048, 256, 8, 512, 512, qm.QS_BF16)
+    need = 144 * 3 * 512 * 2048 // 256
+    ex = qm.make_q4k_experts(fake, need)
+    sh = qm.make_shared(fake, fake, fake, fake)
+    assert L.qs_moe_ffn_q4k(B(shape), fake, fake, None, B(qm.make_q4k_experts(fake, need - 16)), B(sh), fake, 1,
+                            fake, 1 << 30, None) == INV          # stride below the expert's Q4_K bytes
+    assert L.qs_moe_ffn_q4k(B(shape), fake, fake, None, B(qm.make_q4k_experts(fake + 8, need)), B(sh), fake, 1,
+                            fake, 1 << 30, None) == INV          # misaligned blocks
+    assert L.qs_moe_ffn_q4k(B(shape), None, fake, None, B(ex), B(sh), fake, 1, fake, 1 << 30, None) == INV
+    assert L.qs_moe_ffn_q4k(B(shape), fake, fake, None, B(ex), B(sh), fake, 0, fake, 1 << 30, None) == INV
+    assert L.qs_moe_ffn_q4k(B(shape), fake, fake, None, B(ex), B(sh), fake, 1, None, 1 << 30, None) == WS
+    assert L.qs_moe_ffn_q4k(B(shape), fake, fake, None, B(ex), B(sh), fake, 1, fake, 64, None) == WS
+    assert L.qs_q4k_quantize(fake, 4, 100, fake, None) == INV
+    assert L.qs_q4k_quantize(fake + 4, 4, 256, fake, None) == INV
+    assert L.qs_q4k_quantize(fake, 0, 256, fake, None) == INV

@@ -102,8 +102,10 @@ def test_quantize_layer_expert_bit_exact():
 
 # ------------------------------------------------------------------ (a) routing
 
-@pytest.mark.parametrize("wl,T", [("tiny", 4), ("tiny", 13), ("decode_35b_a3b", 64), ("verify8_zipf", 64),
-                                  ("decode_h4096", 24)])
+# decode_35b_a3b at 6 tokens stages exactly 48 KB of x in shared memory (the routing kernel
+# has static shared memory too, so the launch needs the opt-in); at 7, 56 KB.
+@pytest.mark.parametrize("wl,T", [("tiny", 4), ("tiny", 13), ("decode_35b_a3b", 6), ("decode_35b_a3b", 7),
+                                  ("decode_35b_a3b", 64), ("verify8_zipf", 64), ("decode_h4096", 24)])
 def test_route_topk_parity(wl, T):
     w = qi.WORKLOADS[wl]
     L = Layer(w.shape, w.seed, 0, n_x=T, zipf=w.zipf_bias, shared=False, expert_subset=[])
