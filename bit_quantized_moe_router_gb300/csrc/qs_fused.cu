@@ -7,19 +7,23 @@
 // (griddepcontrol.wait) the producer warp only prefetches weights into L2; no
 // thread touches x, the workspace or the output before that wait.  A CTA has
 // one producer warp and 16 consumer warps.  The producer streams the CTA's
-// tiles from HBM into a ring of 21 KB shared-memory stages with bulk
-// asynchronous copies (TMA engine): one "full" mbarrier per stage counts the
-// bytes in, one "empty" mbarrier per stage tells the producer the stage may
-// be refilled.  Tiles, in the order every CTA walks them (tile i of the grid
-// belongs to CTA i mod gridDim):
+// routing-independent tiles from HBM into a ring of 21 KB shared-memory stages
+// with bulk asynchronous copies (TMA engine): one "full" mbarrier per stage
+// counts the bytes in, one "empty" mbarrier per stage tells the producer the
+// stage may be refilled.  Tiles, in the order every CTA walks them (tile i of
+// the grid belongs to CTA i mod gridDim):
 //
-//   router rows (fp32)  |  shared gate/up rows (bf16)  |  [routed gate/up rows (Q2_K)]  |  down groups
+//   router rows (fp32)  |  shared gate/up rows (bf16)  |  [routed gate/up rows (Q2_K)]  |  [down groups]
 //
-// The routed gate/up rows are numbered as tiles but do not pass through the ring:
-// the warps that use them load them from global memory into registers, after
-// each warp has requested all of its rows into L2 at once (one SM's copy engine
-// works through its copies one after another; the load path keeps far more of
-// them in flight).
+// The routed gate/up rows and the down groups (RD output rows: the shared
+// expert's bf16 down rows and every active expert's Q2_K down rows) are
+// numbered as tiles but do not pass through the ring: the warps that use them
+// load them from global memory into registers, after the CTA's warps have
+// requested all of the routed rows into L2 at once (the shared expert's down
+// rows are prefetched at the start).  One SM's copy engine works through its
+// copies one after another, and a down group of many experts would be many
+// copies of a few hundred bytes held in stages while long tasks run; the load
+// path keeps far more of them in flight.
 // Consumers work as independent warp tasks, so different warps can be in
 // different phases at once and nothing waits on a CTA-wide barrier:
 //   group A (warps 0-7):  router rows -> logits; then the routing
@@ -201,8 +205,6 @@ struct Plan {
     int tpe;                  // routed gate/up tiles per active expert
     int n_dg;                 // down groups
     int rowH, rowF;           // Q2_K row bytes along H and along F
-    int bs, be;               // bytes of a down group's shared part / one expert's down rows
-    int m0, mf;               // experts in the first / in a further down sub-tile
     int own_rt, own_st;       // tiles of each kind this CTA owns
     int cpr, rpw, ept;        // Q2_K chunks per gate/up row, rows per task, tasks per tile
     int cpf, epp;             // chunks per down row, experts per warp pass
@@ -228,10 +230,6 @@ __device__ __forceinline__ Plan make_plan(const FusedParams& P) {
     L.n_dg = P.H / P.RD;
     L.rowH = P.H / kBlockWeights * kBlockBytes;
     L.rowF = P.F / kBlockWeights * kBlockBytes;
-    L.bs = P.S > 0 ? P.RD * P.S * 2 : 0;
-    L.be = P.RD * L.rowF;
-    L.m0 = (kStageBytes - L.bs) / L.be;
-    L.mf = kStageBytes / L.be;
     L.own_rt = owned_count(0, L.n_rt, L.G, L.cta);
     L.own_st = owned_count(L.n_rt, L.n_ind, L.G, L.cta);
     L.cpr = 4 * (P.H / kBlockWeights);
@@ -240,22 +238,6 @@ __device__ __forceinline__ Plan make_plan(const FusedParams& P) {
     L.cpf = 4 * (P.F / kBlockWeights);
     L.epp = 32 / L.cpf;
     return L;
-}
-
-__device__ __forceinline__ int down_subtiles(int n_active, const Plan& L) {
-    const int rest = n_active - L.m0;
-    return 1 + (rest > 0 ? (rest + L.mf - 1) / L.mf : 0);
-}
-
-// expert range [a0, a1) of down sub-tile s
-__device__ __forceinline__ void down_sub_range(int s, int n_active, const Plan& L, int& a0, int& a1) {
-    if (s == 0) {
-        a0 = 0;
-        a1 = min(n_active, L.m0);
-    } else {
-        a0 = L.m0 + (s - 1) * L.mf;
-        a1 = min(n_active, a0 + L.mf);
-    }
 }
 
 // ------------------------------------------------------------------ waits (bounded, warp-uniform outcome)
@@ -399,47 +381,6 @@ __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
         }
         __syncwarp();
         seq++;
-    }
-    // the routing, published by group A
-    if (!warp_wait_mbar(C, &C.routed_bar, 0)) {
-        if (lane == 0) vstore(&C.abort, 1);
-        goto done;
-    }
-    {
-        const int na = C.n_active;
-        const int n_et = na * L.tpe;
-        const int lo_dg = L.n_ind + n_et, hi_dg = lo_dg + L.n_dg;
-        const int64_t down_off = 2ll * P.F * L.rowH;
-        // down groups: nsub consecutive stages each
-        const int nsub = down_subtiles(na, L);
-#pragma unroll 1
-        for (int g = first_owned(lo_dg, L.G, L.cta); g < hi_dg; g += L.G) {
-            const int r0 = (g - lo_dg) * P.RD;
-#pragma unroll 1
-            for (int s = 0; s < nsub; s++) {
-                if (!producer_slot(C, seq, ns)) goto done;
-                int a0, a1;
-                down_sub_range(s, na, L, a0, a1);
-                const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
-                if (lane == 0) mbar_arrive_expect_tx(bar(seq), sh + (uint32_t)(a1 - a0) * L.be);
-                __syncwarp();
-                // copy c = 0 is the shared part (sub-tile 0 only), c >= 1 the experts
-#pragma unroll 1
-                for (int c = lane; c < 1 + (a1 - a0); c += 32) {
-                    fence_proxy_async_smem();
-                    if (c == 0) {
-                        if (sh) bulk_g2s(slot(seq), P.sd + (size_t)r0 * P.S, sh, bar(seq));
-                    } else {
-                        const int a = a0 + c - 1;
-                        bulk_g2s(slot(seq) + sh + (size_t)(c - 1) * L.be,
-                                 P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF,
-                                 (uint32_t)L.be, bar(seq));
-                    }
-                }
-                __syncwarp();
-                seq++;
-            }
-        }
     }
 done:
     if (lane == 0) vstore(&C.issued, seq);
@@ -814,9 +755,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int own_et = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta);
         const int lo_dg = L.n_ind + n_et;
         const int own_dg = owned_count(lo_dg, lo_dg + L.n_dg, L.G, L.cta);
-        const int nsub = down_subtiles(na, L);
-        const int seq_et = L.own_rt + L.own_st;       // stage sequence number of the first routed tile
-        const int seq_dg = seq_et;                    // ... of the first down group (routed rows bypass the ring)
         const int n_stage_tasks = (S > 0 ? 1 : 0) + n_ent;
         const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
         const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
@@ -833,6 +771,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             for (int l = lane; l < 2 * lines; l += 32) {
                 const uint8_t* p = row0 + (l >= lines ? (int64_t)P.F * L.rowH : 0) + (int64_t)(l % lines) * 128;
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            }
+        }
+        // ... and every routed down row of this CTA's down groups (RD rows of each active expert)
+        {
+            const int64_t down_off = 2ll * P.F * L.rowH;
+            const int lines = (P.RD * L.rowF + 127) / 128 + 1;  // + 1: the rows need not start on a line
+            const int n_pf = own_dg * na;
+#pragma unroll 1
+            for (int q = warp; ok && q < n_pf; q += kCW) {
+                const int m = q / na, a = q % na;
+                const int r0 = (first_owned(lo_dg, L.G, L.cta) + m * L.G - lo_dg) * P.RD;
+                const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF;
+                const uint8_t* lim = row0 + (int64_t)P.RD * L.rowF;
+                for (int l = lane; l < lines; l += 32) {  // the last one lands on the range's last byte
+                    const uint8_t* p = row0 + (int64_t)l * 128;
+                    if (p >= lim) p = lim - 1;
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+                }
             }
         }
 #pragma unroll 1
@@ -959,45 +915,41 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const int m = dq / P.RD, r = dq % P.RD;
                 const int g = first_owned(lo_dg, L.G, L.cta) + m * L.G;
                 const int r0 = (g - lo_dg) * P.RD;
-                const int sq0 = seq_dg + m * nsub;
-#pragma unroll 1
-                for (int s = 0; ok && s < nsub; s++) ok = warp_wait_tile(C, sq0 + s, ns);
                 if (ok && S > 0) ok = warp_wait_mbar(C, &C.hs_bar, 0);
                 if (ok) ok = warp_wait_mbar(C, &C.staged_bar, 0);
                 if (!ok) break;
-                // routed experts: epp experts per pass, cpf lanes per expert row
+                // routed experts: epp experts per pass, cpf lanes per expert row; a pass's row
+                // chunks are requested before the previous pass is computed
                 const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
                 const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
                 float* pb = pbuf + warp * kMaxEnt;
                 const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
+                const int u = c0 & 3;
+                const uint8_t* rowbase =
+                    P.experts + 2ll * P.F * L.rowH + (int64_t)(r0 + r) * L.rowF + (c0 >> 2) * kBlockBytes;
+                Q2Chunk cur{}, nxt{};
+                if (al < na) load_q2chunk_global(rowbase + (int64_t)C.act_e[al] * P.stride, u, cur);
 #pragma unroll 1
-                for (int s = 0; s < nsub; s++) {
-                    const uint8_t* st = stages + (size_t)((sq0 + s) % ns) * kStageBytes;
-                    int a0, a1;
-                    down_sub_range(s, na, L, a0, a1);
-                    const uint32_t sh = (s == 0) ? (uint32_t)L.bs : 0u;
+                for (int pa = 0; pa < na; pa += L.epp) {
+                    const int a = pa + al;
+                    if (a + L.epp < na) load_q2chunk_global(rowbase + (int64_t)C.act_e[a + L.epp] * P.stride, u, nxt);
+                    if (a < na) {
 #pragma unroll 1
-                    for (int pa = a0; pa < a1; pa += L.epp) {
-                        const int a = pa + al;
-                        if (a < a1) {
-                            const int b = c0 >> 2, u = c0 & 3;
-                            const uint8_t* row = st + sh + (size_t)(a - a0) * L.be + (size_t)r * L.rowF + b * kBlockBytes;
-#pragma unroll 1
-                            for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                                const int ent = C.ent_sorted[j];
-                                XFrag f;
-                                load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
-                                float v = q2k_chunk_dot(row, u, f);
-                                for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
-                                if (c0 == 0) pb[j] = v * C.hscale[ent];
-                            }
+                        for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                            const int ent = C.ent_sorted[j];
+                            XFrag f;
+                            load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
+                            float v = q2k_chunk_dot(cur, u, f);
+                            for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
+                            if (c0 == 0) pb[j] = v * C.hscale[ent];
                         }
                     }
+                    cur = nxt;
                 }
                 // shared expert down row
                 float sacc[MAXT];
                 if (S > 0)
-                    warp_dense_row<MAXT>(stages + (size_t)(sq0 % ns) * kStageBytes + (size_t)r * S * 2, false, S,
+                    warp_dense_row<MAXT>(reinterpret_cast<const uint8_t*>(P.sd + (size_t)(r0 + r) * S), false, S,
                                          reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
                 __syncwarp();
 #pragma unroll
@@ -1013,8 +965,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         P.out[(size_t)t * H + r0 + r] = acc;
                     }
                 }
-#pragma unroll 1
-                for (int s = 0; s < nsub; s++) release_slot(C, (sq0 + s) % ns, P.RD);
             }
         }
         if (!ok) fail(C, status);
@@ -1067,15 +1017,13 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
         while (S % fp.RS) fp.RS--;
     }
     fp.R = 128 / nbH;
-    const int rowF = nbF * 84;
     const int rd_align = 4 / std::min(nbF, 4);
-    const int na_max = std::min(E, T * k);
     int RD = kMaxRD;
-    while (RD > rd_align && (RD * (2 * S + na_max * rowF) > kStageBytes || H / RD < 4 * n_sm)) RD /= 2;
+    // down groups of RD output rows: at least four per CTA (their rows are loaded from global
+    // memory by the warps that use them, not staged)
+    while (RD > rd_align && H / RD < 4 * n_sm) RD /= 2;
     while (RD > H) RD /= 2;
     if (RD < rd_align || H % RD) return false;
-    if (RD * 2 * S > kStageBytes || RD * rowF > kStageBytes) return false;
-    if (S > 0 && RD * 2 * S + RD * rowF > kStageBytes) return false;  // sub-tile 0 holds shared + >= 1 expert
     fp.RD = RD;
     // region 0: x as given and w_sg (phase 1) -- later the int16 h cache
     size_t o = up16((size_t)T * H * xsz);
@@ -1095,11 +1043,6 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
     if (fixed + 2 * (size_t)kStageBytes > smem_max) return false;
     fp.nstages = (int)std::min<size_t>(kMaxStages, (smem_max - fixed) / kStageBytes);
     fp.smem = fixed + (size_t)fp.nstages * kStageBytes;
-    // a down task holds every sub-tile of its group at once: they must fit the ring with room to spare
-    const int bs = S > 0 ? RD * S * 2 : 0, be = RD * rowF;
-    const int m0 = (kStageBytes - bs) / be, mf = kStageBytes / be;
-    const int nsub_max = 1 + (na_max > m0 ? (na_max - m0 + mf - 1) / mf : 0);
-    if (nsub_max > fp.nstages - 1) return false;
     return true;
 }
 
