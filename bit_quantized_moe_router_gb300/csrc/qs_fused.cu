@@ -850,7 +850,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             } else if (q < q_et + n_stage_tasks) {
                 // ---------------------------------------------- staging of hs / of one entry's int16 h
                 const int sidx = q - q_et;
-                // the int16 h cache aliases x and w_sg: wait until their last reader is done
+                // the int16 h cache aliases x, w_sg and the int16 x fragments: wait until group B is
+                // done with x and w_sg; the fragments' last reader, this CTA's last routed gate/up
+                // task, ends before the CTA publishes its h, so entries are staged only after the
+                // h counter below
                 if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
                 if (!(ok = warp_wait_mbar(C, &C.shared_bar, 0))) break;
                 if (S > 0 && sidx == 0) {
@@ -1025,14 +1028,16 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
     while (RD > H) RD /= 2;
     if (RD < rd_align || H % RD) return false;
     fp.RD = RD;
-    // region 0: x as given and w_sg (phase 1) -- later the int16 h cache
+    // region 0: x as given, w_sg and the int16 x fragments -- later the int16 h cache (x and
+    // w_sg are dead once group B has finished its shared gate/up rows; the x fragments once this
+    // CTA's last routed gate/up task has ended, which is before the CTA publishes its h)
     size_t o = up16((size_t)T * H * xsz);
     fp.off_sig = (int)o;
     o += up16((size_t)H * 2);
-    fp.off_hq = 0;
-    o = std::max(o, up16((size_t)T * k * (F / 64) * kFragWords * 4));
     fp.off_xq = (int)o;
     o += up16((size_t)T * (H / 64) * kFragWords * 4);
+    fp.off_hq = 0;
+    o = std::max(o, up16((size_t)T * k * (F / 64) * kFragWords * 4));
     fp.off_hsf = (int)o;
     o += up16((size_t)T * S * 4);
     fp.off_pbuf = (int)o;
@@ -1040,7 +1045,7 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
     o = (o + 127) / 128 * 128;
     fp.off_stages = (int)o;
     const size_t fixed = (sizeof(FusedCtl) + 127) / 128 * 128 + o;
-    if (fixed + 2 * (size_t)kStageBytes > smem_max) return false;
+    if (fixed + (size_t)kStageBytes > smem_max) return false;  // one stage at least (router and shared rows)
     fp.nstages = (int)std::min<size_t>(kMaxStages, (smem_max - fixed) / kStageBytes);
     fp.smem = fixed + (size_t)fp.nstages * kStageBytes;
     return true;
