@@ -413,8 +413,8 @@ __device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int
     const int wsz = w_f32 ? 4 : 2, asz = a_f32 ? 4 : 2;
 #pragma unroll
     for (int t = 0; t < MAXT; t++) acc[t] = 0.0f;
-#pragma unroll 1
-    for (int i = lane * 8; i < K; i += 256) {
+#pragma unroll 4
+    for (int i = lane * 8; i < K; i += 256) {  // unrolled: rows read from global memory keep loads in flight
         float wv[8];
         load8(w + (size_t)i * wsz, w_f32, wv);
 #pragma unroll
