@@ -770,36 +770,36 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
         const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
         bool xq_seen = false;
-        // every routed gate/up row this warp will read, requested at once (lines into L2)
-#pragma unroll 1
-        for (int q = warp; ok && q < q_et; q += kCW) {
-            const int m = q / L.ept, rt = q % L.ept;
-            const int idx = first_owned(L.n_ind, L.G, L.cta) + m * L.G - L.n_ind;
-            const int a = idx / L.tpe, tt = idx % L.tpe;
-            const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw) * L.rowH;
-            const int lines = (L.rpw * L.rowH + 127) / 128;  // rows of the task are contiguous
-#pragma unroll 1
-            for (int l = lane; l < 2 * lines; l += 32) {
-                const uint8_t* p = row0 + (l >= lines ? (int64_t)P.F * L.rowH : 0) + (int64_t)(l % lines) * 128;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-            }
-        }
-        // ... and every routed down row of this CTA's down groups (RD rows of each active expert)
+        // every routed gate/up row and every routed down row this CTA will read, requested into L2
+        // at once, one 128-byte line per consumer thread at a time (gate/up lines first, in task order)
         {
+            const int lines_gu = (L.rpw * L.rowH + 127) / 128;  // per task and matrix (its rows are contiguous)
+            const int n_gu = q_et * 2 * lines_gu;
             const int64_t down_off = 2ll * P.F * L.rowH;
-            const int lines = (P.RD * L.rowF + 127) / 128 + 1;  // + 1: the rows need not start on a line
-            const int n_pf = own_dg * na;
+            const int lines_d = (P.RD * L.rowF + 127) / 128 + 1;  // + 1: the rows need not start on a line
+            const int n_d = own_dg * na * lines_d;
+            const int f_et = first_owned(L.n_ind, L.G, L.cta), f_dg = first_owned(lo_dg, L.G, L.cta);
 #pragma unroll 1
-            for (int q = warp; ok && q < n_pf; q += kCW) {
-                const int m = q / na, a = q % na;
-                const int r0 = (first_owned(lo_dg, L.G, L.cta) + m * L.G - lo_dg) * P.RD;
-                const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF;
-                const uint8_t* lim = row0 + (int64_t)P.RD * L.rowF;
-                for (int l = lane; l < lines; l += 32) {  // the last one lands on the range's last byte
-                    const uint8_t* p = row0 + (int64_t)l * 128;
-                    if (p >= lim) p = lim - 1;
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+            for (int i = tid; ok && i < n_gu + n_d; i += kCT) {
+                const uint8_t* p;
+                if (i < n_gu) {
+                    const int q = i / (2 * lines_gu), l = i % (2 * lines_gu);
+                    const int m = q / L.ept, rt = q % L.ept;
+                    const int idx = f_et + m * L.G - L.n_ind;
+                    const int a = idx / L.tpe, tt = idx % L.tpe;
+                    p = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw) * L.rowH +
+                        (l >= lines_gu ? (int64_t)P.F * L.rowH : 0) + (int64_t)(l % lines_gu) * 128;
+                } else {
+                    const int j = i - n_gu;
+                    const int q = j / lines_d, l = j % lines_d;
+                    const int m = q / na, a = q % na;
+                    const int r0 = (f_dg + m * L.G - lo_dg) * P.RD;
+                    const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF;
+                    const uint8_t* lim = row0 + (int64_t)P.RD * L.rowF;
+                    p = row0 + (int64_t)l * 128;
+                    if (p >= lim) p = lim - 1;  // the last line lands on the range's last byte
                 }
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             }
         }
 #pragma unroll 1
