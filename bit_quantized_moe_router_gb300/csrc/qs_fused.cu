@@ -551,11 +551,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 // per 32-logit chunk: sort, keep the first k as candidates
                 const int chunks = (E + 31) / 32;
                 const int kc = min(k, 32);
+                const int nq = T * chunks;
+                // a warp's chunks one after another; each chunk's logits are loaded while the
+                // previous chunk is sorted
+                auto chunk_logit = [&](int q) {
+                    const int e = (q % chunks) * 32 + lane;
+                    return e < E ? ld_relaxed_f32(P.xlog + (size_t)(q / chunks) * E + e) : -INFINITY;
+                };
+                float vnext = gwarp < nq ? chunk_logit(gwarp) : -INFINITY;
 #pragma unroll 1
-                for (int q = gwarp; q < T * chunks; q += kGW) {
-                    const int t = q / chunks, ch = q % chunks;
-                    const int e = ch * 32 + lane;
-                    float v = e < E ? ld_relaxed_f32(P.xlog + (size_t)t * E + e) : -INFINITY;
+                for (int q = gwarp; q < nq; q += kGW) {
+                    const int e = (q % chunks) * 32 + lane;
+                    float v = vnext;
+                    if (q + kGW < nq) vnext = chunk_logit(q + kGW);
                     if (v != v) v = -INFINITY;  // a NaN logit ranks last
                     int i = e < E ? e : 0x7fffffff;
                     warp_sort32(v, i);
