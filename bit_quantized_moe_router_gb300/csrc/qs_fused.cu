@@ -937,6 +937,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const int m = dq / P.RD, r = dq % P.RD;
                 const int g = first_owned(lo_dg, L.G, L.cta) + m * L.G;
                 const int r0 = (g - lo_dg) * P.RD;
+                // the shared expert's down row is read after the routed passes: request it into L1 now
+                if (S > 0 && lane * 128 < S * 2) {
+                    const uint16_t* srow = P.sd + (size_t)(r0 + r) * S;
+                    for (int l = lane; l * 128 < S * 2; l += 32)
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
+                }
                 if (ok && S > 0) ok = warp_wait_mbar(C, &C.hs_bar, 0);
                 if (ok) ok = warp_wait_mbar(C, &C.staged_bar, 0);
                 if (!ok) break;
