@@ -165,6 +165,7 @@ __device__ __forceinline__ bool warp_wait_tag(const int* tag, int want, volatile
         if (*t != want) {
             const uint64_t t0 = global_timer_ns();
             while (*t != want) {
+                __nanosleep(64);
                 if (*abort) {
                     ok = 0;
                     break;
