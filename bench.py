@@ -104,16 +104,20 @@ def peaks():
 # ------------------------------------------------------------------ distributed plumbing
 
 class Dist:
-    def __init__(self, n_gpus):
+    """One process per GPU under torchrun (NCCL); `backend="gloo"` runs the same host logic on CPU."""
+
+    def __init__(self, n_gpus, backend="nccl"):
         import torch
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = None
+        self.device = "cuda" if backend == "nccl" else "cpu"
         if self.world > 1:
             import torch.distributed as dist
-            torch.cuda.set_device(self.local)
-            dist.init_process_group("nccl")
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
             self.pg = dist
         elif n_gpus > 1:
             raise SystemExit("--gpus > 1 needs torchrun (one process per GPU)")
@@ -126,9 +130,14 @@ class Dist:
         if not self.pg:
             return v
         import torch
-        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        t = torch.tensor([v], dtype=torch.float64, device=self.device)
         self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
         return float(t.item())
+
+
+def aggregate_throughput(tokens_per_rank_step, steps, world, slowest_seconds):
+    """Whole-job tokens/s of independent replicas: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / slowest_seconds
 
 
 # ------------------------------------------------------------------ clocks
@@ -519,7 +528,7 @@ def run_ours(args, w, T):
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     achieved = algo_bytes / mean_step_s / 1e9
     tokens_total = T * K * dist.world
-    value = tokens_total / total_s
+    value = aggregate_throughput(T, K, dist.world, total_s)
     if dist.rank != 0:
         return
     cpu = None
