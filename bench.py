@@ -7,7 +7,11 @@ call of the whole layer (router, top-k, grouping, routed gate/up + SwiGLU,
 down + combine, gated shared expert) on the step's tokens.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--tokens T]
-                  [--impl ours|reference] [--no-flush]
+                  [--impl ours|reference] [--l2 cycle|flush] [--format q2k|q4k] [--steer S]
+
+--format q4k runs the layer with Q4_K routed experts (qs_moe_ffn_q4k); --steer S adds the
+directional steering of every output row (qs_steer_rows) to each step and reports the
+steering kernel alone beside the line.
 
 Timing: W untimed warm-up steps, then K steps.  Inputs are resident in HBM.
 Default (--l2 cycle): inputs larger than L2 -- enough distinct layer copies are
@@ -25,8 +29,8 @@ from pinned host memory and y copied back, all inside one event pair.
 
 Weights are drawn N(0, 0.02) on the device with torch's seeded generator
 (expert weights then quantised by the library's Q2_K encoder, shared weights
-rounded to bf16); x and the Zipf router bias come from the shared seeded
-generators (qs_inputs).
+rounded to bf16); x, the Zipf router bias and the steering direction come from the
+shared seeded generators (qs_inputs).
 `--impl reference` times the oracle (plain C, double precision) on the host
 cores on the same workload: that is this layer's reference implementation.
 """
