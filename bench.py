@@ -489,22 +489,39 @@ def run_ours(args, w, T):
         fl, _, _ = timed("flush", w.copies, False)
         flush_ms = fl / K
 
-    # e2e through the public API: pinned host x in, y back out, inside the events
+    # e2e through the public API: pinned host x in, y back out, inside the events.  The Q2_K
+    # layer takes host buffers itself (qs_moe_ffn_host queues both copies around the layer);
+    # the Q4_K layer and the steered layer copy with torch around their device-buffer calls.
     x_host = torch.from_numpy(xwrap.view(np.int16) if xwrap.dtype == np.uint16 else xwrap).pin_memory()
     y_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
     x_stage = torch.empty_like(xdev[:T])
+    host_api = args.format == "q2k" and not args.steer
+    ws_host = qm.alloc_host_workspace(shape, T) if host_api else None
+
+    def e2e_step(i):
+        j = (i * T) % qi.X_POOL
+        if host_api:
+            Ld = layers[i % len(layers)]
+            qm.qs_moe_ffn_host(shape, x_host[j:j + T], Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], y_host, T,
+                               ws_host, stream)
+        else:
+            x_stage.copy_(x_host[j:j + T], non_blocking=True)
+            step(i, x=x_stage)
+            y_host.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(2e6 + 160000 * K))
     e2e_a, e2e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_a.record(stream)
     for i in range(K):
-        j = ((args.warmup + i) * T) % qi.X_POOL
-        x_stage.copy_(x_host[j:j + T], non_blocking=True)
-        step(args.warmup + i, x=x_stage)
-        y_host.copy_(out, non_blocking=True)
+        e2e_step(args.warmup + i)
     e2e_b.record(stream)
     torch.cuda.synchronize()
     e2e_s = dist.max(e2e_a.elapsed_time(e2e_b) / 1e3)
+    if ws_host is not None and qm.qs_read_device_status(ws_host, stream) != qm.QS_OK:
+        raise SystemExit("device status after the e2e steps: " + qm.status_string(qm.qs_read_device_status(ws_host)))
 
     steer = None
     if args.steer:
@@ -576,7 +593,9 @@ def run_ours(args, w, T):
             "note": "%d layer copies, L2 flushed between steps outside the events (kernel code evicted too)" % w.copies},
         "e2e": {"value": tokens_total / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_stage.numel() * x_stage.element_size()),
-                "d2h_bytes_per_step": int(out.numel() * out.element_size())},
+                "d2h_bytes_per_step": int(out.numel() * out.element_size()),
+                "api": "qs_moe_ffn_host (pinned host x and y)" if host_api else
+                       "device-buffer call with torch copies of pinned host x and y around it"},
         "gpu_launches": launches_per_step * K,
         "kernels_per_step": launches_per_step,
         "clocks": clk,

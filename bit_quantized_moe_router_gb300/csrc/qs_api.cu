@@ -108,6 +108,17 @@ size_t qs_moe_workspace_bytes(const qs_moe_shape* shape, int max_tokens) {
     return ws_layout(*shape, max_tokens).total;
 }
 
+// Host-buffer variant: the layer's workspace, then x's device copy, then out's device copy.
+static size_t host_x_bytes(const qs_moe_shape& s, int T) {
+    return (size_t)T * s.hidden * (s.x_dtype == QS_BF16 ? 2 : 4);
+}
+
+size_t qs_moe_host_workspace_bytes(const qs_moe_shape* shape, int max_tokens) {
+    if (!shape_ok(shape) || max_tokens < 1) return 0;
+    return ws_layout(*shape, max_tokens).total + up256(host_x_bytes(*shape, max_tokens)) +
+           up256((size_t)max_tokens * shape->hidden * 4);
+}
+
 int qs_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
     if (!workspace || workspace_bytes < (size_t)kHeaderBytes || ((uintptr_t)workspace & 255u)) return QS_ERR_WORKSPACE;
     cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, (cudaStream_t)stream);
@@ -239,6 +250,26 @@ int qs_moe_ffn(const qs_moe_shape* shape, const void* x, const float* router_w, 
     if (e != cudaSuccess) return cuda_fail(e);
     e = launch_down(*shape, blocks, experts->expert_stride, ws_at<float>(workspace, L.h), ids, pw, shape->top_k,
                     has_shared ? (const uint16_t*)shared->w_down : nullptr, hs, gate, n_tokens, out, 0, st);
+    return e == cudaSuccess ? QS_OK : cuda_fail(e);
+}
+
+int qs_moe_ffn_host(const qs_moe_shape* shape, const void* x_host, const float* router_w, const float* router_bias,
+                    const qs_q2k_experts* experts, const qs_shared_expert* shared, float* out_host, int n_tokens,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (!shape_ok(shape) || !x_host || !out_host || n_tokens < 1) return QS_ERR_INVALID;
+    if (!workspace || ((uintptr_t)workspace & 255u)) return QS_ERR_WORKSPACE;
+    if (workspace_bytes < qs_moe_host_workspace_bytes(shape, n_tokens)) return QS_ERR_WORKSPACE;
+    const size_t ws_bytes = ws_layout(*shape, n_tokens).total;
+    const size_t xb = host_x_bytes(*shape, n_tokens);
+    uint8_t* x_dev = static_cast<uint8_t*>(workspace) + ws_bytes;
+    float* out_dev = reinterpret_cast<float*>(x_dev + up256(xb));
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int rc = qs_moe_ffn(shape, x_dev, router_w, router_bias, experts, shared, out_dev, n_tokens, workspace,
+                              ws_bytes, stream);
+    if (rc != QS_OK) return rc;
+    e = cudaMemcpyAsync(out_host, out_dev, (size_t)n_tokens * shape->hidden * 4, cudaMemcpyDeviceToHost, st);
     return e == cudaSuccess ? QS_OK : cuda_fail(e);
 }
 

@@ -22,7 +22,8 @@ EXPORTS = (
     "qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes", "qs_workspace_init",
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
     "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
-    "qs_moe_ffn_noalloc", "qs_steer_rows", "qs_moe_ffn_q4k", "qs_q4k_quantize",
+    "qs_moe_ffn_noalloc", "qs_steer_rows", "qs_moe_ffn_q4k", "qs_q4k_quantize", "qs_moe_host_workspace_bytes",
+    "qs_moe_ffn_host",
 )
 
 
@@ -92,8 +93,12 @@ def load(build_if_missing: bool = True):
     L.qs_steer_rows.argtypes = [P, P, ctypes.c_float, i32, i32, P]
     L.qs_moe_ffn_q4k.argtypes = [SP, P, P, P, ctypes.POINTER(qs_q4k_experts), HP, P, i32, P, sz, P]
     L.qs_q4k_quantize.argtypes = [P, i64, i64, P, P]
+    L.qs_moe_host_workspace_bytes.restype = sz
+    L.qs_moe_host_workspace_bytes.argtypes = [SP, i32]
+    L.qs_moe_ffn_host.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
     for name in EXPORTS:
-        if name not in ("qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes"):
+        if name not in ("qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes",
+                        "qs_moe_host_workspace_bytes"):
             getattr(L, name).restype = i32
     _lib = L
     return L
@@ -214,6 +219,25 @@ def qs_steer_rows(out, direction, scale, n_tokens, stream=None):
     """In place, per row of out [n_tokens, hidden] fp32: y <- y - scale * direction * (direction . y)."""
     _check(load().qs_steer_rows(_ptr(out), _ptr(direction), float(scale), n_tokens, out.shape[-1],
                                 _stream(stream)), "qs_steer_rows")
+
+
+def qs_moe_ffn_host(shape, x_host, router_w, router_bias, experts: qs_q2k_experts, shared, out_host, n_tokens,
+                    workspace, stream=None):
+    """The whole layer with x_host and out_host in (pinned) host memory; copies are queued on the stream."""
+    _check(load().qs_moe_ffn_host(ctypes.byref(shape), _ptr(x_host), _ptr(router_w), _ptr(router_bias),
+                                  ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
+                                  _ptr(out_host), n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)), "qs_moe_ffn_host")
+
+
+def alloc_host_workspace(shape: qs_moe_shape, max_tokens: int, device="cuda"):
+    """A zero-initialised workspace for qs_moe_ffn_host."""
+    n = load().qs_moe_host_workspace_bytes(ctypes.byref(shape), max_tokens)
+    if n == 0:
+        raise QsError(QS_ERR_INVALID, "qs_moe_host_workspace_bytes")
+    ws = torch.zeros(n, dtype=torch.uint8, device=device)
+    assert ws.data_ptr() % 256 == 0
+    return ws
 
 
 def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:

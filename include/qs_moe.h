@@ -249,6 +249,20 @@ int qs_q4k_quantize(const float *w, int64_t n_rows, int64_t K, void *out, void *
  * owns both buffers. */
 int qs_steer_rows(float *out, const float *direction, float scale, int n_tokens, int hidden, void *stream);
 
+/* The whole layer with x and out in host memory: queues on `stream` a copy of
+ * x (host, [n_tokens x H], x_dtype) into the workspace, the qs_moe_ffn call
+ * and a copy of the result into out_host (host fp32 [n_tokens x H]), then
+ * returns; synchronise the stream before reading out_host.  Host buffers
+ * should be pinned (page-locked) for the copies to be asynchronous.  Weights,
+ * shared expert and workspace are device memory as for qs_moe_ffn;
+ * workspace: qs_moe_host_workspace_bytes(shape, n_tokens) bytes, 256-byte
+ * aligned, initialised with qs_workspace_init (the layer's workspace first,
+ * then the device copies of x and out).  Errors as qs_moe_ffn. */
+size_t qs_moe_host_workspace_bytes(const qs_moe_shape *shape, int max_tokens);
+int qs_moe_ffn_host(const qs_moe_shape *shape, const void *x_host, const float *router_w, const float *router_bias,
+                    const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out_host, int n_tokens,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
 /* Number of kernels one qs_moe_ffn call with this shape, token count and
  * shared expert (has_shared != 0) launches on the current device: 1 for the
  * persistent decode kernel, 8 for the tensor-core path (which also issues a

@@ -119,3 +119,21 @@ def test_q4k_arguments_are_checked_before_any_launch():
     assert L.qs_q4k_quantize(fake, 4, 100, fake, None) == INV
     assert L.qs_q4k_quantize(fake + 4, 4, 256, fake, None) == INV
     assert L.qs_q4k_quantize(fake, 0, 256, fake, None) == INV
+
+
+def test_host_buffer_call_checks_before_any_copy():
+    L = qm.load()
+    fake = 1 << 40
+    B = ctypes.byref
+    INV, WS = qm.QS_ERR_INVALID, qm.QS_ERR_WORKSPACE
+    shape = qm.make_shape(2048, 256, 8, 512, 512, qm.QS_BF16)
+    ex = qm.make_experts(fake, 1032192)
+    sh = qm.make_shared(fake, fake, fake, fake)
+    need = L.qs_moe_host_workspace_bytes(B(shape), 4)
+    assert need > L.qs_moe_workspace_bytes(B(shape), 4) + 4 * 2048 * 2 + 4 * 2048 * 4 - 1
+    assert L.qs_moe_ffn_host(B(shape), None, fake, None, B(ex), B(sh), fake, 4, fake, need, None) == INV
+    assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), None, 4, fake, need, None) == INV
+    assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 0, fake, need, None) == INV
+    assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, fake, need - 256, None) == WS
+    assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, fake + 16, need, None) == WS
+    assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, None, need, None) == WS
