@@ -23,7 +23,9 @@ launches lengthens the gap between them, so per-step events would time
 themselves too).  --l2 flush: 4 copies, and between timed steps the L2 is
 flushed (512 MiB write + 256 MiB read) outside the step's own events; this
 also evicts the kernel's own code, so it is the pessimistic figure; it is
-reported beside the default as `l2_flush`.  Time is max over ranks.  `e2e`
+reported beside the default as `l2_flush`, with the 10th, 50th and 90th percentile
+of its per-step times.  `graph`: the same K steps captured in one CUDA graph and
+replayed once inside one event pair.  Time is max over ranks.  `e2e`
 times the same K calls through the public API with each step's x copied in
 from pinned host memory and y copied back, all inside one event pair.
 
@@ -412,13 +414,13 @@ def run_ours(args, w, T):
 
     direction = torch.from_numpy(qi.gen_direction(H, w.seed)).to(device)
 
-    def step(i, x=None, n_layers=None):
+    def step(i, x=None, n_layers=None, stream_=None):
         Ld = layers[i % (n_layers or len(layers))]
         ffn = qm.qs_moe_ffn_q4k if args.format == "q4k" else qm.qs_moe_ffn
-        ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T,
-                      ws, stream)
+        st_ = stream if stream_ is None else stream_
+        ffn(shape, xs(i) if x is None else x, Ld["Wr"], Ld["bias"], Ld["experts"], Ld["shared"], out, T, ws, st_)
         if args.steer:
-            qm.qs_steer_rows(out, direction, args.steer, T, stream)
+            qm.qs_steer_rows(out, direction, args.steer, T, st_)
 
     # distinct experts per step (routing is a function of the copy and the x rows)
     ids = torch.empty((T, sh.top_k), dtype=torch.int32, device=device)
@@ -476,18 +478,53 @@ def run_ours(args, w, T):
         dist.barrier()
         clk = clocks.stop() if clocks else None
         if mode == "flush":
-            return float(sum(a.elapsed_time(b) for a, b in evs)), wall, clk
-        return float(evs[0][0].elapsed_time(evs[0][1])), wall, clk
+            per_step = [a.elapsed_time(b) for a, b in evs]
+            return float(sum(per_step)), wall, clk, per_step
+        return float(evs[0][0].elapsed_time(evs[0][1])), wall, clk, None
 
-    total_ms, wall, clk = timed(args.l2, None, True)
+    total_ms, wall, clk, _ = timed(args.l2, None, True)
     total_s = dist.max(total_ms / 1e3)
     st = qm.qs_read_device_status(ws, stream)
     if st != qm.QS_OK:
         raise SystemExit(f"device status after the timed steps: {qm.status_string(st)}")
-    flush_ms = None
+    flush_ms = flush_pct = None
     if args.l2 == "cycle":
-        fl, _, _ = timed("flush", w.copies, False)
+        fl, _, _, per_step = timed("flush", w.copies, False)
         flush_ms = fl / K
+        flush_pct = [float(np.percentile(per_step, q)) * 1e3 for q in (10, 50, 90)]
+
+    # the same K steps captured in one CUDA graph and replayed (eager launches above); the
+    # layer's launches keep their programmatic-dependency edges inside the graph
+    graph = None
+    try:
+        cap = torch.cuda.Stream(device=device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for i in range(args.warmup):
+                step(i, stream_=cap)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(K):
+                step(args.warmup + i, stream_=cap)
+        g.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize()
+        g_s = dist.max(ga.elapsed_time(gb) / 1e3)
+        graph = {"us_per_layer": g_s / K * 1e6, "value": aggregate_throughput(T, K, dist.world, g_s),
+                 "note": "the K timed steps captured in one CUDA graph, one replay timed (launches from the "
+                         "graph instead of the host; same layer copies and x rows)"}
+        del g
+    except RuntimeError as exc:   # capture refused (QsError is one too): report it, keep the eager figures
+        torch.cuda.synchronize()
+        graph = {"error": str(exc).splitlines()[0][:200]}
+    st = qm.qs_read_device_status(ws, stream)
+    if st != qm.QS_OK:
+        raise SystemExit(f"device status after the graph replay: {qm.status_string(st)}")
 
     # e2e through the public API: pinned host x in, y back out, inside the events.  The Q2_K
     # layer takes host buffers itself (qs_moe_ffn_host queues both copies around the layer);
@@ -590,7 +627,10 @@ def run_ours(args, w, T):
         "roofline": roof,
         "l2_flush": None if flush_ms is None else {
             "us_per_layer": flush_ms * 1e3, "frac": algo_bytes / (flush_ms / 1e3) / 1e9 / hbm_peak,
-            "note": "%d layer copies, L2 flushed between steps outside the events (kernel code evicted too)" % w.copies},
+            "p10_us": flush_pct[0], "p50_us": flush_pct[1], "p90_us": flush_pct[2],
+            "note": "%d layer copies, L2 flushed between steps outside the events (kernel code evicted too); "
+                    "per-step events" % w.copies},
+        "graph": graph,
         "e2e": {"value": tokens_total / e2e_s, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_stage.numel() * x_stage.element_size()),
                 "d2h_bytes_per_step": int(out.numel() * out.element_size()),
