@@ -43,7 +43,27 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(const void* __r
     const int chunk = blockIdx.y;
     const int t0 = chunk * kRouteTok;
     const int nt = min(kRouteTok, T - t0);
-    for (int i = threadIdx.x; i < nt * H; i += blockDim.x) xs[i] = load_x(x, x_dtype, (size_t)t0 * H + i);
+    // the token chunk, 8 values per 16-byte (bf16) or 32-byte (fp32) group; each thread issues
+    // up to four groups' loads before it stores any, so the staging is one round trip per batch
+    const int ng = nt * H / 8;
+#pragma unroll 1
+    for (int g0 = threadIdx.x; g0 < ng; g0 += 4 * blockDim.x) {
+        float v[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int g = g0 + u * blockDim.x;
+            if (g < ng) load8_x(x, x_dtype, (size_t)t0 * H + (size_t)g * 8, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; u++) {
+            const int g = g0 + u * blockDim.x;
+            if (g < ng) {
+                float4* d = reinterpret_cast<float4*>(xs + (size_t)g * 8);
+                d[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                d[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+            }
+        }
+    }
     __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * kRouteWarps + warp;
@@ -52,16 +72,30 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(const void* __r
 #pragma unroll
         for (int t = 0; t < kRouteTok; t++) acc[t] = 0.0f;
         const float4* w4 = reinterpret_cast<const float4*>(W + (size_t)e * H);
-        for (int i = lane; i < H / 4; i += 32) {
-            const float4 w = __ldg(w4 + i);
+        const int n4 = H / 4;
+        // eight loads of the row in flight per lane, then the FMAs in the same element order
+#pragma unroll 1
+        for (int i0 = lane; i0 < n4; i0 += 32 * 8) {
+            float4 w[8];
 #pragma unroll
-            for (int t = 0; t < kRouteTok; t++) {
-                if (t < nt) {
-                    const float4 xv = reinterpret_cast<const float4*>(xs + t * H)[i];
-                    acc[t] = fmaf(w.x, xv.x, acc[t]);
-                    acc[t] = fmaf(w.y, xv.y, acc[t]);
-                    acc[t] = fmaf(w.z, xv.z, acc[t]);
-                    acc[t] = fmaf(w.w, xv.w, acc[t]);
+            for (int u = 0; u < 8; u++) {
+                const int i = i0 + 32 * u;
+                w[u] = i < n4 ? __ldg(w4 + i) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; u++) {
+                const int i = i0 + 32 * u;
+                if (i < n4) {
+#pragma unroll
+                    for (int t = 0; t < kRouteTok; t++) {
+                        if (t < nt) {
+                            const float4 xv = reinterpret_cast<const float4*>(xs + t * H)[i];
+                            acc[t] = fmaf(w[u].x, xv.x, acc[t]);
+                            acc[t] = fmaf(w[u].y, xv.y, acc[t]);
+                            acc[t] = fmaf(w[u].z, xv.z, acc[t]);
+                            acc[t] = fmaf(w[u].w, xv.w, acc[t]);
+                        }
+                    }
                 }
             }
         }

@@ -20,10 +20,11 @@
 //                        of x over each 32-weight sub-block are staged; a warp
 //                        takes a row, a lane a sub-block (lanes stride over the
 //                        row's sub-blocks), one fixed shuffle reduction
-//   q4k_down_kernel      CTA per (tile of 16 output rows, token); the token's k
-//                        rows of h and their sub-block sums are staged; a warp
-//                        takes a row and sums the k slots' dot products, each
-//                        weighted by its routing weight, in slot order
+//   q4k_down_kernel      CTA per (tile of 4 or 16 output rows, token); the token's
+//                        k rows of h and their sub-block sums are staged; a warp
+//                        takes a (row, slot) pair's dot product; one thread per
+//                        row sums the k slots' dots, each weighted by its routing
+//                        weight, in slot order
 // Per 32-weight sub-block the dot is sum(q*x) in fp32 (one FMA per weight after
 // the nibble is extracted) and the sub-block result d*sc*sum(q*x) - dmin*m*sum(x).
 #include "qs_common.cuh"
@@ -161,9 +162,23 @@ __device__ __forceinline__ float q4k_sub_dot(const uint8_t* blk, int j, const fl
 }
 
 // Stage a row of n activations as fp32 and the sum of each 32-value group (block-wide).
+// Each thread issues up to eight loads before it stores any of them.
 template <class Load>
 __device__ __forceinline__ void stage_row(Load ld, int n, float* a, float* asum) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) a[i] = ld(i);
+#pragma unroll 1
+    for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int i = i0 + u * blockDim.x;
+            v[u] = i < n ? ld(i) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; u++) {
+            const int i = i0 + u * blockDim.x;
+            if (i < n) a[i] = v[u];
+        }
+    }
     __syncthreads();
     for (int g = threadIdx.x; g < n / 32; g += blockDim.x) {
         float s = 0.0f;
@@ -280,16 +295,19 @@ __global__ void __launch_bounds__(kQ4Threads) q4k_gateup_kernel(const void* __re
 
 // ====================================================================== down + routing-weight combine
 
-constexpr int kQ4DownRows = 16;
+constexpr int kQ4DownRowsMax = 16;
 
-// grid (H / 16, T); block kQ4Threads.  dynamic smem: h f32[k][F] | h sums f32[k][F/32] |
-// slot expert i32[k] | slot weight f32[k].  out[t, r] = sum over slots (in slot order) of
-// p * (Wd_e h) -- stored, not added.
-__global__ void __launch_bounds__(kQ4Threads) q4k_down_kernel(int H, int k, int F, const uint8_t* __restrict__ experts,
+// grid (H / rows, T); block kQ4Threads; rows is 4 or 16 (a divisor of H).  dynamic smem:
+// h f32[k][F] | h sums f32[k][F/32] | slot expert i32[k] | slot weight f32[k].  A warp
+// takes (row, slot) pairs and leaves each dot in shared memory; then one thread per row
+// forms out[t, r] = sum over slots (in slot order) of p * (Wd_e h) -- stored, not added.
+__global__ void __launch_bounds__(kQ4Threads) q4k_down_kernel(int H, int k, int F, int rows,
+                                                              const uint8_t* __restrict__ experts,
                                                               int64_t stride, const float* __restrict__ h,
                                                               const int32_t* __restrict__ ids,
                                                               const float* __restrict__ pw, float* __restrict__ out) {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ float dots[kQ4DownRowsMax * 32];  // [row][slot], k <= 32
     float* ha = reinterpret_cast<float*>(smem);
     float* hsum = ha + (size_t)k * F;
     int32_t* se = reinterpret_cast<int32_t*>(hsum + (size_t)k * (F / 32));
@@ -304,15 +322,19 @@ __global__ void __launch_bounds__(kQ4Threads) q4k_down_kernel(int H, int k, int 
     }
     const float* ht = h + (size_t)t * k * F;
     stage_row([&](int i) { return ht[i]; }, k * F, ha, hsum);
-    for (int rr = warp; rr < kQ4DownRows; rr += kQ4Threads / 32) {
-        const int r = blockIdx.x * kQ4DownRows + rr;
+#pragma unroll 1
+    for (int q = warp; q < rows * k; q += kQ4Threads / 32) {
+        const int rr = q / k, j = q - rr * k;
+        const int r = blockIdx.x * rows + rr;
+        const uint8_t* row = experts + (int64_t)se[j] * stride + 2ll * F * rb_h + (int64_t)r * rb_f;
+        const float v = q4k_row_dot(row, nbf, ha + (size_t)j * F, hsum + (size_t)j * (F / 32));
+        if (lane == 0) dots[rr * 32 + j] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < rows) {
         float acc = 0.0f;
-        for (int j = 0; j < k; j++) {
-            const uint8_t* row = experts + (int64_t)se[j] * stride + 2ll * F * rb_h + (int64_t)r * rb_f;
-            const float v = q4k_row_dot(row, nbf, ha + (size_t)j * F, hsum + (size_t)j * (F / 32));
-            acc = fmaf(sp[j], v, acc);
-        }
-        if (lane == 0) out[(size_t)t * H + r] = acc;
+        for (int j = 0; j < k; j++) acc = fmaf(sp[j], dots[threadIdx.x * 32 + j], acc);
+        out[(size_t)t * H + blockIdx.x * rows + threadIdx.x] = acc;
     }
 }
 
@@ -350,9 +372,12 @@ cudaError_t launch_q4k_down(const qs_moe_shape& s, const uint8_t* experts, int64
     const size_t smem = q4k_down_smem(s.top_k, s.expert_ffn);
     cudaError_t err = q4_set_smem((const void*)q4k_down_kernel, smem);
     if (err != cudaSuccess) return err;
-    dim3 grid(s.hidden / kQ4DownRows, T);
-    q4k_down_kernel<<<grid, kQ4Threads, smem, st>>>(s.hidden, s.top_k, s.expert_ffn, experts, stride, h, ids, pw,
-                                                    out);
+    // few tokens: 4 output rows per CTA, so that the grid covers the SMs; many tokens: 16, so
+    // that the h rows each CTA stages are shared by more output rows
+    const int rows = T <= 16 ? 4 : kQ4DownRowsMax;
+    dim3 grid(s.hidden / rows, T);
+    q4k_down_kernel<<<grid, kQ4Threads, smem, st>>>(s.hidden, s.top_k, s.expert_ffn, rows, experts, stride, h, ids,
+                                                    pw, out);
     return cudaGetLastError();
 }
 
