@@ -31,6 +31,22 @@ namespace qs {
 
 constexpr int kRouteWarps = 2;  // expert rows per router CTA (one warp each)
 
+// Eight consecutive activations from element i (a multiple of 8; x 16-byte aligned), widened.
+__device__ __forceinline__ void load8_x(const void* x, int x_dtype, size_t i, float* v) {
+    if (x_dtype == QS_BF16) {
+        const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + i);
+        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+        v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+        v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+    } else {
+        const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + i);
+        const float4 a = p[0], b = p[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+}
+
 // grid (ceil(E / kRouteWarps), ceil(T / kRouteTok)), block 32 * kRouteWarps.
 // dynamic smem: kRouteTok * H floats (the token chunk, widened to fp32).
 __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(const void* __restrict__ x, int x_dtype,
