@@ -133,9 +133,20 @@ cudaError_t launch_q4k_quantize(const float* w, int64_t n_blocks, uint8_t* out, 
 
 constexpr int kQ4Threads = 256;
 
+// Staged activation rows.  A row of K activations (nsub = K/32 sub-blocks) is kept as
+// float4 groups ordered [w][s]: group w (values 4w..4w+3) of sub-block s is float4 number
+// w * nsub + s.  A lane that owns sub-block s reads groups w = 0..7 in order, so at each
+// step the lanes of a warp (consecutive s) read consecutive 16-byte groups.
+__device__ __forceinline__ int q4_stage_pos(int e, int nsub) {
+    const int sb = e >> 5, c = e & 31;
+    return (((c >> 2) * nsub + sb) << 2) | (c & 3);
+}
+
 // Dot of one 32-weight sub-block j of the 16-byte-aligned block `blk` (global or shared
-// memory) with 32 activations a[0..31] (shared memory) whose sum is asum.
-__device__ __forceinline__ float q4k_sub_dot(const uint8_t* blk, int j, const float* a, float asum) {
+// memory) with the 32 activations of sub-block s of a staged row a4 (nsub sub-blocks,
+// shared memory) whose sum is asum.
+__device__ __forceinline__ float q4k_sub_dot(const uint8_t* blk, int j, const float4* a4, int nsub, int s,
+                                             float asum) {
     const uint4 hdr = *reinterpret_cast<const uint4*>(blk);
     const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
     const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
@@ -147,11 +158,10 @@ __device__ __forceinline__ float q4k_sub_dot(const uint8_t* blk, int j, const fl
     const int sh = 4 * (j & 1);
     const uint4 q0 = qs[0], q1 = qs[1];
     const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    const float4* a4 = reinterpret_cast<const float4*>(a);
     float acc = 0.0f;
 #pragma unroll
     for (int w = 0; w < 8; w++) {
-        const float4 x = a4[w];
+        const float4 x = a4[w * nsub + s];
         const uint32_t v = qw[w] >> sh;
         acc = fmaf((float)(v & 15u), x.x, acc);
         acc = fmaf((float)((v >> 8) & 15u), x.y, acc);
@@ -161,10 +171,12 @@ __device__ __forceinline__ float q4k_sub_dot(const uint8_t* blk, int j, const fl
     return d * (float)sc * acc - dm * (float)mn * asum;
 }
 
-// Stage a row of n activations as fp32 and the sum of each 32-value group (block-wide).
-// Each thread issues up to eight loads before it stores any of them.
+// Stage n activations (rows of K, K a multiple of 256) as fp32 in the [w][s] order above,
+// and the sum of each 32-value sub-block, added in element order (block-wide).  Each
+// thread issues up to eight loads before it stores any of them.
 template <class Load>
-__device__ __forceinline__ void stage_row(Load ld, int n, float* a, float* asum) {
+__device__ __forceinline__ void stage_row(Load ld, int n, int K, float* a, float* asum) {
+    const int nsub = K >> 5;
 #pragma unroll 1
     for (int i0 = threadIdx.x; i0 < n; i0 += 8 * blockDim.x) {
         float v[8];
@@ -176,14 +188,19 @@ __device__ __forceinline__ void stage_row(Load ld, int n, float* a, float* asum)
 #pragma unroll
         for (int u = 0; u < 8; u++) {
             const int i = i0 + u * blockDim.x;
-            if (i < n) a[i] = v[u];
+            if (i < n) {
+                const int r = i / K, e = i - r * K;
+                a[(size_t)r * K + q4_stage_pos(e, nsub)] = v[u];
+            }
         }
     }
     __syncthreads();
     for (int g = threadIdx.x; g < n / 32; g += blockDim.x) {
+        const int r = g / nsub, sb = g - r * nsub;
+        const float* row = a + (size_t)r * K;
         float s = 0.0f;
 #pragma unroll 8
-        for (int i = 0; i < 32; i++) s += a[32 * g + i];
+        for (int i = 0; i < 32; i++) s += row[q4_stage_pos(32 * sb + i, nsub)];
         asum[g] = s;
     }
     __syncthreads();
@@ -198,9 +215,11 @@ __device__ __forceinline__ float load_x_f32(const void* x, int x_dtype, size_t i
 // 8*nb sub-blocks; one fixed butterfly sum over the warp.  Every lane gets the result.
 __device__ __forceinline__ float q4k_row_dot(const uint8_t* row, int nb, const float* a, const float* asum) {
     const int lane = threadIdx.x & 31;
+    const float4* a4 = reinterpret_cast<const float4*>(a);
+    const int nsub = 8 * nb;
     float acc = 0.0f;
-    for (int s = lane; s < 8 * nb; s += 32)
-        acc += q4k_sub_dot(row + (size_t)(s >> 3) * kQ4Bytes, s & 7, a + 32 * s, asum[s]);
+    for (int s = lane; s < nsub; s += 32)
+        acc += q4k_sub_dot(row + (size_t)(s >> 3) * kQ4Bytes, s & 7, a4, nsub, s, asum[s]);
     return warp_sum(acc);
 }
 
@@ -271,7 +290,7 @@ __global__ void __launch_bounds__(kQ4Threads) q4k_gateup_kernel(const void* __re
     for (int j = j0; j < j1; j++) {
         const int entry = perm[j];
         const int t = entry / k;
-        stage_row([&](int i) { return load_x_f32(x, x_dtype, (size_t)t * H + i); }, H, xa, xsum);
+        stage_row([&](int i) { return load_x_f32(x, x_dtype, (size_t)t * H + i); }, H, H, xa, xsum);
         if (!waited) {
             if (threadIdx.x == 0) S.ok = mbar_wait(&S.bar, 0) ? 1 : 0;
             __syncthreads();
@@ -321,7 +340,7 @@ __global__ void __launch_bounds__(kQ4Threads) q4k_down_kernel(int H, int k, int 
         sp[threadIdx.x] = pw[(size_t)t * k + threadIdx.x];
     }
     const float* ht = h + (size_t)t * k * F;
-    stage_row([&](int i) { return ht[i]; }, k * F, ha, hsum);
+    stage_row([&](int i) { return ht[i]; }, k * F, F, ha, hsum);
 #pragma unroll 1
     for (int q = warp; q < rows * k; q += kQ4Threads / 32) {
         const int rr = q / k, j = q - rr * k;
