@@ -258,9 +258,7 @@ __device__ __forceinline__ bool block_mbar_wait(uint64_t* bar, uint32_t parity, 
     if (threadIdx.x == 0) *flag = mbar_wait(bar, parity) ? 1 : 0;
     __syncthreads();
     const bool ok = *flag != 0;
-    if (ok)
-        while (!mbar_try_wait(bar, parity)) {
-        }
+    if (ok) (void)mbar_wait(bar, parity);  // the phase is complete: the first poll succeeds
     return ok;
 }
 

@@ -295,8 +295,9 @@ __global__ void __launch_bounds__(kQ4Threads) q4k_gateup_kernel(const void* __re
             if (threadIdx.x == 0) S.ok = mbar_wait(&S.bar, 0) ? 1 : 0;
             __syncthreads();
             if (!S.ok) return;  // the copy never completed: outputs left unwritten
-            while (!mbar_try_wait(&S.bar, 0)) {
-            }
+            // every thread observes the completed phase (its first poll succeeds), which makes
+            // the copied bytes visible to it
+            (void)mbar_wait(&S.bar, 0);
             waited = true;
         }
         for (int r = warp; r < R; r += kQ4Threads / 32) {
