@@ -219,17 +219,24 @@ def oracle_sample_layer(w, T, n_tokens, copy=0, fmt="q2k"):
     return xb, Wr, bias, shared, blob
 
 
-def time_oracle(w, T, budget_s, max_calls=None, fmt="q2k"):
-    """Run the oracle, one layer call of T tokens at a time on one core, for ~budget_s seconds."""
+def oracle_threads():
+    """Host threads for the oracle on many-token calls: every core, at most 64."""
+    return max(1, min(64, os.cpu_count() or 1))
+
+
+def time_oracle(w, T, budget_s, max_calls=None, fmt="q2k", threads=1):
+    """Run the oracle for ~budget_s seconds: layer calls of T tokens (at most 16) on one
+    thread, or with threads > 1 calls of 2 tokens per thread, the tokens split over them."""
     import oracle
-    T = min(T, ORACLE_TOKENS_MAX)
+    T = min(T, ORACLE_TOKENS_MAX) if threads == 1 else 2 * threads
     n_pool = 16 if T == 1 else max(T, 16)
     xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool, fmt=fmt)
     calls, tokens = 0, 0
     t0 = time.perf_counter()
     while True:
         t_start = (calls * T) % max(1, n_pool - T + 1)
-        oracle.moe_ffn(w.shape, xb[t_start:t_start + T], Wr, bias, blob, expert_bytes(w.shape, fmt), shared, fmt=fmt)
+        oracle.moe_ffn(w.shape, xb[t_start:t_start + T], Wr, bias, blob, expert_bytes(w.shape, fmt), shared, fmt=fmt,
+                       threads=threads)
         calls += 1
         tokens += T
         el = time.perf_counter() - t0
@@ -258,14 +265,17 @@ def run_reference(args, w, T):
     import oracle
     oracle.build()
     T_full = T
-    T = min(T, ORACLE_TOKENS_MAX)
+    # decode batches: one thread, the call's own tokens; many tokens: calls of 2 tokens per
+    # host thread, the tokens split over every core
+    nth = oracle_threads() if T_full > ORACLE_TOKENS_MAX else 1
+    T = 2 * nth if nth > 1 else min(T, ORACLE_TOKENS_MAX)
     n_pool = max(T, 16)
     xb, Wr, bias, shared, blob = oracle_sample_layer(w, T, n_pool, fmt=args.format)
 
     def step(i):
         t0 = (i * T) % max(1, n_pool - T + 1)
         oracle.moe_ffn(w.shape, xb[t0:t0 + T], Wr, bias, blob, expert_bytes(w.shape, args.format), shared,
-                       fmt=args.format)
+                       fmt=args.format, threads=nth)
 
     for i in range(args.warmup):
         step(i)
@@ -282,9 +292,10 @@ def run_reference(args, w, T):
         "us_per_layer": ms * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
         "config": config_of(w, T_full, args),
-        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nth, "kind": "oracle",
                          "sample": f"{args.steps} layer calls of {T} token(s) over a {n_pool}-token x pool, "
                                    f"experts those tokens route to"
+                                   + (f", tokens split over {nth} threads" if nth > 1 else "")
                                    + (f" (the oracle's cost per token does not depend on the batch of {T_full})"
                                       if T_full > T else "") + f"; {cpu_model()}"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -591,12 +602,19 @@ def run_ours(args, w, T):
         return
     cpu = None
     if not args.no_cpu_baseline and dist.world == 1:
-        rate, calls, el = time_oracle(w, T, args.cpu_seconds, fmt=args.format)
-        ts = min(T, ORACLE_TOKENS_MAX)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{calls} layer calls of {ts} token(s) ({el:.1f} s, one thread), x pool of 16 tokens and "
-                         f"the experts they route to" + (" (per-token cost independent of the batch)" if T > ts else "")
-                         + f"; {cpu_model()}"}
+        if T > ORACLE_TOKENS_MAX:   # many tokens per call: the tokens split over every host core
+            nth = oracle_threads()
+            rate, calls, el = time_oracle(w, T, args.cpu_seconds, fmt=args.format, threads=nth)
+            r1, c1, e1 = time_oracle(w, T, args.cpu_seconds / 2, fmt=args.format)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                   "sample": f"{calls} layer calls of {2 * nth} tokens split over {nth} threads ({el:.1f} s); "
+                             f"one thread: {r1:.2f} tokens/s ({c1} calls of {ORACLE_TOKENS_MAX} tokens, {e1:.1f} s); "
+                             f"the oracle's cost per token does not depend on the batch; {cpu_model()}"}
+        else:
+            rate, calls, el = time_oracle(w, T, args.cpu_seconds, fmt=args.format)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{calls} layer calls of {T} token(s) ({el:.1f} s, one thread), x pool of 16 tokens "
+                             f"and the experts they route to; {cpu_model()}"}
     if args.format == "q2k" and layer_launches > 1 and T > 16:  # tensor-core path: bound by the 16-bit tensor pipe
         flops = layer_flops(sh, T)
         tf_peak = pk["bf16_tflops"] if pk else 1900.0
