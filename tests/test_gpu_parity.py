@@ -258,6 +258,40 @@ def test_moe_ffn_without_shared_expert():
     check_layer_outputs(L, L.oracle(), got, range(3), "no shared")
 
 
+# ------------------------------------------------------------------ the largest batches and top-k
+
+def test_moe_ffn_decode_kernel_at_its_entry_limit():
+    """16 tokens x top-8 = 128 (token, slot) entries: the most the single-kernel decode path takes
+    (with 64 experts its candidate buffer holds them; its int16 h cache leaves one stage)."""
+    shape = qi.LayerShape(2048, 64, 8, 512, 512, qi.BF16)
+    L = Layer(shape, 310, 0, n_x=16)
+    D = DevLayer(L)
+    assert qm.qs_moe_ffn_launches(D.shape, 16, True) == 1
+    check_layer_outputs(L, L.oracle(threads=8), D.moe(0, 16), range(16), "decode kernel, 128 entries")
+
+
+@pytest.mark.parametrize("T,x_dtype,launches", [(4, qi.BF16, 1), (5, qi.BF16, 8), (5, qi.F32, 5)])
+def test_moe_ffn_top_k_32(T, x_dtype, launches):
+    """top-k at its maximum (32) on each path: the decode kernel (4 x 32 = 128 entries), the
+    tensor-core path (160 entries, bf16 x) and the per-step kernels (fp32 x)."""
+    shape = qi.LayerShape(256, 64, 32, 256, 256, x_dtype)
+    L = Layer(shape, 320 + T, 0, n_x=T)
+    D = DevLayer(L)
+    assert qm.qs_moe_ffn_launches(D.shape, T, True) == launches
+    check_layer_outputs(L, L.oracle(), D.moe(0, T), range(T), f"top-32, {T} tokens, {launches} launches")
+
+
+@pytest.mark.slow
+def test_moe_ffn_35b_shape_between_decode_and_prefill_batches():
+    """The 35B-A3B layer at 12 tokens: past the decode kernel's candidate buffer (8 tokens at 256
+    experts, top-8), below the smallest batch the tensor-core tests take."""
+    w = qi.WORKLOADS["decode_35b_a3b"]
+    L = Layer(w.shape, w.seed, 0, n_x=12, expert_subset="routed")
+    D = DevLayer(L)
+    assert qm.qs_moe_ffn_launches(D.shape, 12, True) == 8
+    check_layer_outputs(L, L.oracle(threads=8), D.moe(0, 12), range(12), "35B-A3B layer, 12 tokens")
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("wl,T,calls", [("decode_35b_a3b", 1, 4), ("verify8_zipf", 8, 1), ("decode_h4096", 1, 2),
                                         ("decode_h4096", 4, 1)])
