@@ -506,7 +506,7 @@ def run_ours(args, w, T):
 
     # the same K steps captured in one CUDA graph and replayed (eager launches above); the
     # layer's launches keep their programmatic-dependency edges inside the graph
-    graph = None
+    g_local, g_err = float("inf"), None
     try:
         cap = torch.cuda.Stream(device=device)
         cap.wait_stream(stream)
@@ -525,14 +525,18 @@ def run_ours(args, w, T):
         g.replay()
         gb.record(stream)
         torch.cuda.synchronize()
-        g_s = dist.max(ga.elapsed_time(gb) / 1e3)
-        graph = {"us_per_layer": g_s / K * 1e6, "value": aggregate_throughput(T, K, dist.world, g_s),
-                 "note": "the K timed steps captured in one CUDA graph, one replay timed (launches from the "
-                         "graph instead of the host; same layer copies and x rows)"}
+        g_local = ga.elapsed_time(gb) / 1e3
         del g
     except RuntimeError as exc:   # capture refused (QsError is one too): report it, keep the eager figures
         torch.cuda.synchronize()
-        graph = {"error": str(exc).splitlines()[0][:200]}
+        g_err = str(exc).splitlines()[0][:200]
+    g_s = dist.max(g_local)       # every rank takes part, whatever happened on it
+    if g_err is not None or not math.isfinite(g_s):
+        graph = {"error": g_err or "graph capture failed on another rank"}
+    else:
+        graph = {"us_per_layer": g_s / K * 1e6, "value": aggregate_throughput(T, K, dist.world, g_s),
+                 "note": "the K timed steps captured in one CUDA graph, one replay timed (launches from the "
+                         "graph instead of the host; same layer copies and x rows)"}
     st = qm.qs_read_device_status(ws, stream)
     if st != qm.QS_OK:
         raise SystemExit(f"device status after the graph replay: {qm.status_string(st)}")
