@@ -108,11 +108,25 @@ def status_string(code: int) -> str:
     return load().qs_status_string(code).decode()
 
 
-def _ptr(t):
-    if t is None:
-        return None
-    if isinstance(t, int):
+def _dptr(t):
+    """Address of a contiguous CUDA tensor; None and raw integer addresses pass through."""
+    if t is None or isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a tensor in device memory, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _hptr(t):
+    """Address of a contiguous host tensor (pinned, for asynchronous copies)."""
+    if t is None or isinstance(t, int):
+        return t
+    if t.is_cuda:
+        raise ValueError("expected a tensor in host memory, got one on the device")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
     return t.data_ptr()
 
 
@@ -134,15 +148,15 @@ def make_shape(hidden, n_experts, top_k, expert_ffn, shared_ffn, x_dtype) -> qs_
 
 
 def make_experts(blocks, expert_stride: int) -> qs_q2k_experts:
-    return qs_q2k_experts(_ptr(blocks), expert_stride)
+    return qs_q2k_experts(_dptr(blocks), expert_stride)
 
 
 def make_q4k_experts(blocks, expert_stride: int) -> qs_q4k_experts:
-    return qs_q4k_experts(_ptr(blocks), expert_stride)
+    return qs_q4k_experts(_dptr(blocks), expert_stride)
 
 
 def make_shared(w_gate, w_up, w_down, w_gate_sig) -> qs_shared_expert:
-    return qs_shared_expert(_ptr(w_gate), _ptr(w_up), _ptr(w_down), _ptr(w_gate_sig))
+    return qs_shared_expert(_dptr(w_gate), _dptr(w_up), _dptr(w_down), _dptr(w_gate_sig))
 
 
 # ------------------------------------------------------------------ entry points
@@ -160,73 +174,73 @@ def qs_moe_workspace_bytes(shape: qs_moe_shape, max_tokens: int) -> int:
 
 
 def qs_workspace_init(workspace, stream=None):
-    _check(load().qs_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().qs_workspace_init(_dptr(workspace), workspace.numel() * workspace.element_size(),
                                     _stream(stream)), "qs_workspace_init")
 
 
 def qs_read_device_status(workspace, stream=None) -> int:
-    return load().qs_read_device_status(_ptr(workspace), _stream(stream))
+    return load().qs_read_device_status(_dptr(workspace), _stream(stream))
 
 
 def qs_route_topk(shape, x, router_w, router_bias, n_tokens, topk_ids, topk_w, workspace, stream=None):
-    _check(load().qs_route_topk(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias), n_tokens,
-                                _ptr(topk_ids), _ptr(topk_w), _ptr(workspace),
+    _check(load().qs_route_topk(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias), n_tokens,
+                                _dptr(topk_ids), _dptr(topk_w), _dptr(workspace),
                                 workspace.numel() * workspace.element_size(), _stream(stream)), "qs_route_topk")
 
 
 def qs_group_tokens(shape, topk_ids, n_tokens, counts, offsets, perm, stream=None):
-    _check(load().qs_group_tokens(ctypes.byref(shape), _ptr(topk_ids), n_tokens, _ptr(counts), _ptr(offsets),
-                                  _ptr(perm), _stream(stream)), "qs_group_tokens")
+    _check(load().qs_group_tokens(ctypes.byref(shape), _dptr(topk_ids), n_tokens, _dptr(counts), _dptr(offsets),
+                                  _dptr(perm), _stream(stream)), "qs_group_tokens")
 
 
 def qs_q2k_gemv_grouped(shape, x, experts: qs_q2k_experts, offsets, perm, n_tokens, h_out, stream=None):
-    _check(load().qs_q2k_gemv_grouped(ctypes.byref(shape), _ptr(x), ctypes.byref(experts), _ptr(offsets),
-                                      _ptr(perm), n_tokens, _ptr(h_out), _stream(stream)), "qs_q2k_gemv_grouped")
+    _check(load().qs_q2k_gemv_grouped(ctypes.byref(shape), _dptr(x), ctypes.byref(experts), _dptr(offsets),
+                                      _dptr(perm), n_tokens, _dptr(h_out), _stream(stream)), "qs_q2k_gemv_grouped")
 
 
 def qs_q2k_down_combine(shape, experts: qs_q2k_experts, h, topk_ids, topk_w, n_tokens, out, accumulate=False,
                         stream=None):
-    _check(load().qs_q2k_down_combine(ctypes.byref(shape), ctypes.byref(experts), _ptr(h), _ptr(topk_ids),
-                                      _ptr(topk_w), n_tokens, _ptr(out), int(bool(accumulate)), _stream(stream)),
+    _check(load().qs_q2k_down_combine(ctypes.byref(shape), ctypes.byref(experts), _dptr(h), _dptr(topk_ids),
+                                      _dptr(topk_w), n_tokens, _dptr(out), int(bool(accumulate)), _stream(stream)),
            "qs_q2k_down_combine")
 
 
 def qs_shared_expert_ffn(shape, x, shared: qs_shared_expert, n_tokens, out, workspace, accumulate=False,
                          stream=None):
-    _check(load().qs_shared_expert_ffn(ctypes.byref(shape), _ptr(x), ctypes.byref(shared), n_tokens, _ptr(out),
-                                       int(bool(accumulate)), _ptr(workspace),
+    _check(load().qs_shared_expert_ffn(ctypes.byref(shape), _dptr(x), ctypes.byref(shared), n_tokens, _dptr(out),
+                                       int(bool(accumulate)), _dptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)),
            "qs_shared_expert_ffn")
 
 
 def qs_moe_ffn(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens, workspace,
                stream=None):
-    _check(load().qs_moe_ffn(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
-                             ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _ptr(out),
-                             n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().qs_moe_ffn(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
+                             ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
+                             n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)), "qs_moe_ffn")
 
 
 def qs_moe_ffn_noalloc(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens,
                        stream=None):
     """The whole layer with its scratch in a fixed array inside the library (no workspace argument)."""
-    _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
+    _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                                      ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
-                                     _ptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
+                                     _dptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
 
 
 def qs_steer_rows(out, direction, scale, n_tokens, stream=None):
     """In place, per row of out [n_tokens, hidden] fp32: y <- y - scale * direction * (direction . y)."""
-    _check(load().qs_steer_rows(_ptr(out), _ptr(direction), float(scale), n_tokens, out.shape[-1],
+    _check(load().qs_steer_rows(_dptr(out), _dptr(direction), float(scale), n_tokens, out.shape[-1],
                                 _stream(stream)), "qs_steer_rows")
 
 
 def qs_moe_ffn_host(shape, x_host, router_w, router_bias, experts: qs_q2k_experts, shared, out_host, n_tokens,
                     workspace, stream=None):
     """The whole layer with x_host and out_host in (pinned) host memory; copies are queued on the stream."""
-    _check(load().qs_moe_ffn_host(ctypes.byref(shape), _ptr(x_host), _ptr(router_w), _ptr(router_bias),
+    _check(load().qs_moe_ffn_host(ctypes.byref(shape), _hptr(x_host), _dptr(router_w), _dptr(router_bias),
                                   ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
-                                  _ptr(out_host), n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _hptr(out_host), n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)), "qs_moe_ffn_host")
 
 
@@ -246,25 +260,25 @@ def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:
 
 def qs_q2k_quantize(w, out, stream=None):
     rows, K = w.shape
-    _check(load().qs_q2k_quantize(_ptr(w), rows, K, _ptr(out), _stream(stream)), "qs_q2k_quantize")
+    _check(load().qs_q2k_quantize(_dptr(w), rows, K, _dptr(out), _stream(stream)), "qs_q2k_quantize")
 
 
 def qs_q4k_quantize(w, out, stream=None):
     rows, K = w.shape
-    _check(load().qs_q4k_quantize(_ptr(w), rows, K, _ptr(out), _stream(stream)), "qs_q4k_quantize")
+    _check(load().qs_q4k_quantize(_dptr(w), rows, K, _dptr(out), _stream(stream)), "qs_q4k_quantize")
 
 
 def qs_moe_ffn_q4k(shape, x, router_w, router_bias, experts: qs_q4k_experts, shared, out, n_tokens, workspace,
                    stream=None):
     """The whole layer with Q4_K routed experts (same arguments as qs_moe_ffn)."""
-    _check(load().qs_moe_ffn_q4k(ctypes.byref(shape), _ptr(x), _ptr(router_w), _ptr(router_bias),
-                                 ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _ptr(out),
-                                 n_tokens, _ptr(workspace), workspace.numel() * workspace.element_size(),
+    _check(load().qs_moe_ffn_q4k(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
+                                 ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
+                                 n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream(stream)), "qs_moe_ffn_q4k")
 
 
 def qs_test_wait_timeout(workspace, limit_us, stream=None):
-    _check(load().qs_test_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(), limit_us,
+    _check(load().qs_test_wait_timeout(_dptr(workspace), workspace.numel() * workspace.element_size(), limit_us,
                                        _stream(stream)), "qs_test_wait_timeout")
 
 

@@ -137,3 +137,23 @@ def test_host_buffer_call_checks_before_any_copy():
     assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, fake, need - 256, None) == WS
     assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, fake + 16, need, None) == WS
     assert L.qs_moe_ffn_host(B(shape), fake, fake, None, B(ex), B(sh), fake, 4, None, need, None) == WS
+
+
+def test_binding_refuses_tensors_on_the_wrong_side():
+    """The binding passes device addresses only for contiguous CUDA tensors and host addresses
+    only for contiguous host tensors; anything else raises before the library is called."""
+    import torch
+    shape = qm.make_shape(256, 8, 2, 256, 256, qm.QS_F32)
+    host = torch.zeros((2, 256), dtype=torch.float32)
+    with pytest.raises(ValueError, match="device memory"):
+        qm.make_experts(torch.zeros(64512 * 8, dtype=torch.uint8), 64512)
+    with pytest.raises(ValueError, match="device memory"):
+        qm.make_shared(host, host, host, host)
+    with pytest.raises(ValueError, match="device memory"):
+        qm.qs_steer_rows(host, torch.zeros(256), 1.0, 2)
+    ex = qm.make_experts(1 << 40, 64512)
+    with pytest.raises(ValueError, match="device memory"):
+        qm.qs_moe_ffn(shape, host, 1 << 40, None, ex, None, 1 << 40, 2, torch.zeros(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="contiguous"):
+        qm._hptr(torch.zeros((256, 2)).t())
+    assert qm._hptr(host) == host.data_ptr() and qm._dptr(1 << 40) == 1 << 40 and qm._dptr(None) is None
