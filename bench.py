@@ -246,14 +246,17 @@ def time_oracle(w, T, budget_s, max_calls=None, fmt="q2k", threads=1):
 
 
 def cpu_model():
+    """The host CPU's model (or architecture) and its core count, for the baseline's sample text."""
+    import platform
+    model = platform.machine()
     try:
         for line in open("/proc/cpuinfo"):
             if line.lower().startswith(("model name", "cpu model")):
-                return line.split(":", 1)[1].strip()
+                model = line.split(":", 1)[1].strip()
+                break
     except Exception:
         pass
-    import platform
-    return platform.machine()
+    return f"{model}, {os.cpu_count() or 1} host cores"
 
 
 def run_reference(args, w, T):
