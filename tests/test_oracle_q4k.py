@@ -110,6 +110,25 @@ def test_dequant_is_the_formula_on_random_fields():
     assert np.array_equal(w.reshape(-1), np.concatenate(exp))
 
 
+def test_quantizer_fixed_point_on_representable_block():
+    # d = 2^-10 and dmin = 2^-11 are exact in fp16; one sub-block has scale 63 and one has min 63,
+    # so d = max(s)/63 and dmin = max(m)/63 come back exactly; every sub-block uses codes 0 and
+    # 15, so its min is -dmin*mc and its max + min is 15*d*sc.  All values are short dyadic
+    # numbers, exact in fp32, and re-encoding must give the same bytes.
+    rng = np.random.default_rng(8)
+    sc = np.array([63, 1, 17, 40, 5, 33, 62, 9], np.uint8)
+    m = np.array([0, 63, 12, 1, 48, 7, 30, 21], np.uint8)
+    q = rng.integers(0, 16, 256).astype(np.uint8)
+    for j in range(8):
+        q[32 * j] = 0
+        q[32 * j + 31] = 15
+    b = oracle.q4k_pack(sc, m, q, 0x1400, 0x1000)   # fp16 bits of 2^-10 and 2^-11
+    w = oracle.q4k_dequant(b, 1, 256)
+    assert np.array_equal(w.astype(np.float32).astype(np.float64), w)
+    again = oracle.q4k_quantize(w.astype(np.float32))
+    assert np.array_equal(again.reshape(-1), b)
+
+
 def test_quantizer_zero_row_gives_zero_block():
     q = oracle.q4k_quantize(np.zeros((1, 256), np.float32))
     assert np.all(oracle.q4k_dequant(q, 1, 256) == 0.0)
