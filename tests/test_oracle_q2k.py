@@ -159,6 +159,27 @@ def test_quantizer_fixed_point_on_representable_block():
     assert np.array_equal(oracle.q2k_dequant(blk, 1, 256)[0], w.astype(np.float64))
 
 
+def test_quantizer_fixed_point_with_an_all_positive_sub_block():
+    # The encoder's min is m = max(0, -min w).  Sub-block 5 has min nibble 0 and codes 1..3
+    # only, so all its weights are positive: its m must be 0 and its step max/3 (an unclamped
+    # min would give the step (max - min)/3 and another scale nibble).  Sub-block 0 carries scale
+    # nibble 15 and sub-block 1 min nibble 15, so d and dmin come back exactly; the other
+    # sub-blocks use codes 0 and 3, so their min is -dmin*hi and their range is 3*d*lo.
+    rng = np.random.default_rng(9)
+    lo = np.array([15, 2, 7, 1, 11, 6, 3, 9, 4, 13, 5, 8, 10, 12, 14, 1], np.uint8)
+    hi = np.array([0, 15, 3, 9, 1, 0, 7, 2, 11, 4, 13, 6, 8, 5, 10, 12], np.uint8)
+    codes = rng.integers(0, 4, 256).astype(np.uint8)
+    for sb in range(16):
+        codes[16 * sb], codes[16 * sb + 15] = 0, 3
+    codes[80:96] = rng.integers(1, 4, 16)
+    codes[80], codes[95] = 1, 3
+    blk = oracle.q2k_pack(lo | (hi << 4), codes, 0x1400, 0x1000)   # d = 2^-10, dmin = 2^-11
+    w = oracle.q2k_dequant(blk, 1, 256)[0]
+    assert np.all(w[80:96] > 0)
+    assert np.array_equal(w.astype(np.float32).astype(np.float64), w)
+    assert np.array_equal(oracle.q2k_quantize(w.astype(np.float32)[None, :])[0], blk)
+
+
 def test_quantizer_zero_row_gives_zero_block():
     blk = oracle.q2k_quantize(np.zeros((1, 256), np.float32))[0]
     assert np.all(blk == 0)

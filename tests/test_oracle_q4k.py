@@ -129,6 +129,26 @@ def test_quantizer_fixed_point_on_representable_block():
     assert np.array_equal(again.reshape(-1), b)
 
 
+def test_quantizer_fixed_point_with_an_all_positive_sub_block():
+    # The encoder's min is m = max(0, -min w).  Sub-block 3 has min 0 and codes 1..15 only, so
+    # all its weights are positive: its m must be 0 and its step max/15 (an unclamped min would
+    # give the step (max - min)/15 and the scale 37 in place of 40).  Scale 63 and min 63 fix d
+    # and dmin as in the fixed point above; the other sub-blocks use codes 0 and 15.
+    rng = np.random.default_rng(10)
+    sc = np.array([63, 1, 17, 40, 5, 33, 62, 9], np.uint8)
+    m = np.array([5, 63, 12, 0, 48, 7, 30, 21], np.uint8)
+    q = rng.integers(0, 16, 256).astype(np.uint8)
+    for j in range(8):
+        q[32 * j], q[32 * j + 31] = 0, 15
+    q[96:128] = rng.integers(1, 16, 32)
+    q[96], q[127] = 1, 15
+    b = oracle.q4k_pack(sc, m, q, 0x1400, 0x1000)   # d = 2^-10, dmin = 2^-11
+    w = oracle.q4k_dequant(b, 1, 256)
+    assert np.all(w[0, 96:128] > 0)
+    assert np.array_equal(w.astype(np.float32).astype(np.float64), w)
+    assert np.array_equal(oracle.q4k_quantize(w.astype(np.float32)).reshape(-1), b)
+
+
 def test_quantizer_zero_row_gives_zero_block():
     q = oracle.q4k_quantize(np.zeros((1, 256), np.float32))
     assert np.all(oracle.q4k_dequant(q, 1, 256) == 0.0)
