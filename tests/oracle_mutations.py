@@ -2,7 +2,7 @@
 
 Each entry below plants one plausible mistake in the oracle (a dropped term, a wrong sign,
 index, divisor or rounding, a swapped or transposed operand), by replacing one exact
-substring of oracle/qs_oracle.c that must occur once.  The mistake goes into a copy of
+substring of oracle/qs_oracle.c (or of the named oracle file) that must occur once.  The mistake goes into a copy of
 oracle/, qs_inputs/ and tests/ in a temporary directory, never into the repository.  Then
 the oracle pins run there (the CPU tests test_oracle_*.py).  Every mutation must make a pin
 fail; one that does not is reported as SURVIVED, and the script exits non-zero.  Every
@@ -76,6 +76,13 @@ M = [
     ("steer sign", "yt[i] = yt[i] - scale * (double)d[i] * c;", "yt[i] = yt[i] + scale * (double)d[i] * c;"),
     ("steer dot operand", "for (int i = 0; i < H; i++) c += (double)d[i] * yt[i];",
      "for (int i = 0; i < H; i++) c += (double)d[i] * d[i];"),
+    # the Python side of the oracle
+    ("threads drop a part", "parts = [todo[i::threads] for i in range(threads)]",
+     "parts = [todo[i::threads] for i in range(threads - 1)]", "oracle/__init__.py"),
+    ("expert blob gate and up swapped", "np.concatenate([qz(gate).reshape(-1), qz(up).reshape(-1), qz(down).reshape(-1)])",
+     "np.concatenate([qz(up).reshape(-1), qz(gate).reshape(-1), qz(down).reshape(-1)])", "oracle/__init__.py"),
+    ("steer scale sign in the wrapper", "lib().qso_steer_rows(H, T, _p(dd), float(scale), _p(yy))",
+     "lib().qso_steer_rows(H, T, _p(dd), float(-scale), _p(yy))", "oracle/__init__.py"),
 ]
 
 TESTS = ["tests/test_oracle_q2k.py", "tests/test_oracle_layer.py", "tests/test_oracle_q4k.py",
@@ -99,18 +106,19 @@ def main():
     only = sys.argv[1:]
     tmp = tempfile.mkdtemp(prefix="oracle_mutations_")
     BASE = os.path.join(tmp, "m")
-    src0 = open(os.path.join(REPO, "oracle", "qs_oracle.c")).read()
     results = []
-    for name, old, new in M:
+    for name, old, new, *where in M:
         if only and name not in only:
             continue
+        rel = where[0] if where else "oracle/qs_oracle.c"
+        src0 = open(os.path.join(REPO, rel)).read()
         n = src0.count(old)
         if n != 1:
             results.append((name, f"BAD PATTERN ({n} matches)"))
             print(name, results[-1][1], flush=True)
             continue
         mirror()
-        open(os.path.join(BASE, "oracle", "qs_oracle.c"), "w").write(src0.replace(old, new))
+        open(os.path.join(BASE, rel), "w").write(src0.replace(old, new))
         env = dict(os.environ, PYTHONPATH=BASE)
         try:
             r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", *TESTS],

@@ -167,6 +167,26 @@ def test_diagonal_expert_gives_elementwise_swiglu():
     assert np.all(y[4:] == 0)
 
 
+def test_expert_blob_keeps_gate_up_down_roles():
+    # Three different matrices for the three roles (gate 2I, up I, down I/2), each quantised on
+    # its own for the expectation: the layer's h and y must follow the matrix each role was made
+    # from, whatever order the expert's blob stores them in.
+    n = 256
+    shape = qi.LayerShape(n, 1, 1, n, 0, qi.F32)
+    eye = np.eye(n, dtype=np.float32)
+    gate, up, down = 2.0 * eye, eye, 0.5 * eye
+    blob = oracle.quantize_expert(gate, up, down)
+    Wg, Wu, Wd = (oracle.q2k_dequant(oracle.q2k_quantize(a), n, n) for a in (gate, up, down))
+    x = np.zeros((1, n), np.float32)
+    x[0, :3] = [1.0, -0.5, 2.0]
+    out = oracle.moe_ffn(shape, x, np.zeros((1, n), np.float32), None, blob, shape.expert_bytes, None)
+    xf = x[0].astype(np.float64)
+    h = _silu(Wg @ xf) * (Wu @ xf)
+    assert not np.allclose(h, _silu(Wu @ xf) * (Wg @ xf))   # the roles are told apart
+    assert np.allclose(out["h"][0], h, rtol=1e-12, atol=1e-15)
+    assert np.allclose(out["y"][0], Wd @ h, rtol=1e-12, atol=1e-15)
+
+
 def test_zero_router_gives_uniform_weights_and_sum_of_mlps():
     shape = qi.LayerShape(256, 4, 2, 256, 0, qi.F32)
     experts, stride = _random_layer(shape, 31)
