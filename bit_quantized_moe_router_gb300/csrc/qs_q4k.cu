@@ -16,10 +16,12 @@
 //   q4k_quantize_kernel  fp32 rows -> blocks, one warp per block (set-up step)
 //   q4k_gateup_kernel    CTA per (active expert, tile of R rows); the tile's gate
 //                        and up rows are staged in shared memory by two bulk
-//                        copies; per routed token, its x row (fp32) and the sums
-//                        of x over each 32-weight sub-block are staged; a warp
-//                        takes a row, a lane a sub-block (lanes stride over the
-//                        row's sub-blocks), one fixed shuffle reduction
+//                        copies; per routed token, its x row (fp32, as float4
+//                        groups ordered [group][sub-block], so that a warp's
+//                        lanes read consecutive groups) and the sums of x over
+//                        each 32-weight sub-block are staged; a warp takes a
+//                        row, a lane a sub-block (lanes stride over the row's
+//                        sub-blocks), one fixed shuffle reduction
 //   q4k_down_kernel      CTA per (tile of 4 or 16 output rows, token); the token's
 //                        k rows of h and their sub-block sums are staged; a warp
 //                        takes a (row, slot) pair's dot product; one thread per
