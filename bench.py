@@ -146,6 +146,20 @@ def aggregate_throughput(tokens_per_rank_step, steps, world, slowest_seconds):
     return tokens_per_rank_step * steps * world / slowest_seconds
 
 
+def graph_result(dist, local_seconds, local_error, tokens_per_rank_step, steps):
+    """The graph-replay figure: every rank takes part in the max over ranks, whatever happened on
+    it (a rank whose capture failed passes +inf), and the figure stands only if every rank's
+    capture worked."""
+    import math
+    slowest = dist.max(local_seconds if local_error is None else float("inf"))
+    if local_error is not None or not math.isfinite(slowest):
+        return {"error": local_error or "graph capture failed on another rank"}
+    return {"us_per_layer": slowest / steps * 1e6,
+            "value": aggregate_throughput(tokens_per_rank_step, steps, dist.world, slowest),
+            "note": "the K timed steps captured in one CUDA graph, one replay timed (launches from the "
+                    "graph instead of the host; same layer copies and x rows)"}
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -533,13 +547,7 @@ def run_ours(args, w, T):
     except RuntimeError as exc:   # capture refused (QsError is one too): report it, keep the eager figures
         torch.cuda.synchronize()
         g_err = str(exc).splitlines()[0][:200]
-    g_s = dist.max(g_local)       # every rank takes part, whatever happened on it
-    if g_err is not None or not math.isfinite(g_s):
-        graph = {"error": g_err or "graph capture failed on another rank"}
-    else:
-        graph = {"us_per_layer": g_s / K * 1e6, "value": aggregate_throughput(T, K, dist.world, g_s),
-                 "note": "the K timed steps captured in one CUDA graph, one replay timed (launches from the "
-                         "graph instead of the host; same layer copies and x rows)"}
+    graph = graph_result(dist, g_local, g_err, T, K)
     st = qm.qs_read_device_status(ws, stream)
     if st != qm.QS_OK:
         raise SystemExit(f"device status after the graph replay: {qm.status_string(st)}")

@@ -49,6 +49,42 @@ def test_two_replicas_take_the_slowest_rank():
         assert value == pytest.approx(4 * 10 * 2 / 1.5)
 
 
+def _graph_rank(rank, world, port, fail_rank, out):
+    os.environ.update({"MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port), "RANK": str(rank),
+                       "WORLD_SIZE": str(world), "LOCAL_RANK": str(rank)})
+    d = bench.Dist(world, backend="gloo")
+    failed = rank == fail_rank
+    res = bench.graph_result(d, float("inf") if failed else 0.002 * (rank + 1), "capture refused" if failed else None,
+                             8, 100)
+    out[rank] = res
+    d.barrier()
+    d.pg.destroy_process_group()
+
+
+@pytest.mark.parametrize("fail_rank", [-1, 1])
+def test_graph_figure_needs_every_rank(fail_rank):
+    """Every rank joins the max over ranks, also one whose graph capture failed, so no rank waits
+    for a collective that another rank skipped; the figure stands only if all captures worked."""
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_graph_rank, args=(r, 2, port, fail_rank, out)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(out)
+    if fail_rank < 0:
+        for r in range(2):
+            assert res[r]["us_per_layer"] == pytest.approx(0.004 / 100 * 1e6)
+            assert res[r]["value"] == pytest.approx(8 * 100 * 2 / 0.004)
+    else:
+        assert res[1] == {"error": "capture refused"}
+        assert res[0] == {"error": "graph capture failed on another rank"}
+
+
 def test_single_process_needs_no_group():
     d = bench.Dist(1, backend="gloo")
     assert d.world == 1 and d.max(3.0) == 3.0
