@@ -127,9 +127,9 @@ def main():
             tail = (r.stdout.strip().splitlines() or [""])[-1]
         except subprocess.TimeoutExpired:
             caught, tail = True, "timeout"
-        verdict = "caught" if caught else "SURVIVED"
-        results.append((name, verdict + " | " + tail))
-        print(f"{name}: {verdict} | {tail}", flush=True)
+        outcome = "caught" if caught else "SURVIVED"
+        results.append((name, outcome + " | " + tail))
+        print(f"{name}: {outcome} | {tail}", flush=True)
     shutil.rmtree(tmp, ignore_errors=True)
     survivors = [n for n, v in results if not v.startswith("caught")]
     print("\nnot caught:", survivors)
