@@ -24,7 +24,7 @@ constexpr uint64_t kWaitNs = 200ull * 1000ull * 1000ull;  // 200 ms: any legitim
 // Workspace header.  Counters live in separate 32-byte sectors.
 struct WsHeader {
     uint32_t status;        // sticky qs_status of device-side failures (0 = ok)
-    uint32_t where[7];      // first time-out of the tensor-core path: wait code, CTA, cluster rank, warp, counter
+    uint32_t where[7];      // first time-out of the tensor-core path: wait code, CTA, warp, counter
     uint32_t ctr[7][8];     // ctr[i][0] = counter i
 };
 static_assert(sizeof(WsHeader) <= kHeaderBytes, "header too large");
@@ -149,28 +149,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// ------------------------------------------------------------------ thread-block clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_count_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster (release / acquire).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Hint: bring a span into L2 (16-byte aligned, multiple of 16 bytes).

@@ -71,7 +71,6 @@ constexpr int kRouterStages = 3;
 constexpr int kRouterThreads = 192;
 constexpr int kMaxKS = kPrefillMaxKS;     // router split of H
 constexpr uint32_t kSleepNs = 20000;      // longest hardware suspension of a waiting thread per poll
-constexpr int kMaxCluster = 1;            // most CTAs sharing B slices by multicast (1: no clusters)
 
 enum RawMode : int { kRawColumn = 0, kRawTile = 1 };
 
@@ -86,16 +85,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
             smem_u32(dst)),
         "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-// The same box written to this CTA-relative offset in every CTA of `cta_mask`, each CTA's
-// mbarrier at `bar`'s offset receiving the completion.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
         : "memory");
 }
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
@@ -116,14 +105,13 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 // Record the first time-out: status = QS_ERR_TIMEOUT and, beside it in the workspace
-// header, which wait gave up (code), in which CTA, cluster rank and warp, at which counter.
+// header, which wait gave up (code), in which CTA and warp, at which counter.
 __device__ __noinline__ void note_timeout(uint32_t* status, uint32_t code, uint32_t counter) {
     if (atomicCAS(status, 0u, (uint32_t)QS_ERR_TIMEOUT) == 0u) {
         status[1] = code;
         status[2] = blockIdx.x;
-        status[3] = cluster_ctarank();
-        status[4] = threadIdx.x >> 5;
-        status[5] = counter;
+        status[3] = threadIdx.x >> 5;
+        status[4] = counter;
         __threadfence();
     }
 }
@@ -509,7 +497,6 @@ struct ExpertParams {
     int MT, MTs;         // 128-row output tiles of the routed / shared matrices
     int E, k, T, F, S, H;
     int n_sgroups;       // shared-expert token tiles (0 when there is no shared expert)
-    int cs;              // CTAs per cluster; they share each token tile's B slices by multicast
     int nt;              // token-tile height (MMA N limit)
     const int32_t* counts;
     const int32_t* offsets;
@@ -556,7 +543,7 @@ struct Unit {
 };
 
 // Unit = (group g, output tile m).  Groups are token tiles: the shared expert's first, then each
-// expert's.  The CTAs of a cluster take the same groups; rank r takes tiles r, r + cs, ...
+// expert's.
 __device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, const ExpertTables& tb) {
     Unit U;
     U.mt = m;
@@ -584,22 +571,14 @@ __device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, c
 }
 
 // Iterate this CTA's units in order: body(U) for each; stop early when body returns false.
+// Units (group-major) are dealt to CTAs one by one, for balance.
 template <class Body>
 __device__ __forceinline__ void for_units(const ExpertParams& p, const ExpertTables& tb, int n_groups, Body body) {
-    if (p.cs == 1) {  // no clusters: units (group-major) dealt to CTAs one by one, for balance
-        const int n_su = p.n_sgroups * p.MTs, n_units = n_su + (n_groups - p.n_sgroups) * p.MT;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const Unit U = (u < n_su) ? make_unit(u / p.MTs, u % p.MTs, p, tb)
-                                      : make_unit(p.n_sgroups + (u - n_su) / p.MT, (u - n_su) % p.MT, p, tb);
-            if (!body(U)) return;
-        }
-        return;
-    }
-    const int rank = (int)cluster_ctarank(), cid = (int)cluster_id_x(), ncl = (int)cluster_count_x();
-    for (int g = cid; g < n_groups; g += ncl) {
-        const int per = ((g < p.n_sgroups) ? p.MTs : p.MT) / p.cs;
-        for (int j = 0; j < per; j++)
-            if (!body(make_unit(g, rank + p.cs * j, p, tb))) return;
+    const int n_su = p.n_sgroups * p.MTs, n_units = n_su + (n_groups - p.n_sgroups) * p.MT;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const Unit U = (u < n_su) ? make_unit(u / p.MTs, u % p.MTs, p, tb)
+                                  : make_unit(p.n_sgroups + (u - n_su) / p.MT, (u - n_su) % p.MT, p, tb);
+        if (!body(U)) return;
     }
 }
 
@@ -647,10 +626,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
     tb.cnts = tb.offs + p.E;
     volatile int* abort = &ctl->abort;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)cluster_ctarank();
-    // B stages are released to this CTA's own barrier and to the cluster leader's, which
-    // counts every CTA of the cluster before it multicasts the stage's next slice.
-    const uint16_t release_mask = (uint16_t)(1u | (1u << rank));
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSA; s++) {
@@ -659,7 +634,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
         for (int s = 0; s < kNB; s++) {
             mbar_init(&ctl->bfull[s], 1);
-            mbar_init(&ctl->bempty[s], rank == 0 ? p.cs : 1);
+            mbar_init(&ctl->bempty[s], 1);
         }
         for (int r = 0; r < kNRv; r++) {
             mbar_init(&ctl->rawfull[r], 1);
@@ -703,7 +678,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
     }
     tc::fence_before();
-    cluster_sync();  // barriers of every CTA initialised before any multicast reaches them
+    __syncthreads();
     tc::fence_after();
     const uint32_t tbase = ctl->tmem;
     const int n_groups = ctl->n_groups;
@@ -920,8 +895,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         }
                         tc::commit(&ctl->aempty[s]);
                     }
-                    if (p.cs > 1) tc::commit_mc(&ctl->bempty[sb], release_mask);
-                    else tc::commit(&ctl->bempty[sb]);
+                    tc::commit(&ctl->bempty[sb]);
                 }
                 tc::commit(&ctl->accfull[b]);
                 GB += g.KB;
@@ -940,7 +914,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             int C = 0, GB = 0;
             int used_d[kNRv] = {}, used_m[kNRv] = {}, last_use[kNRv];  // last consumer: 0 none, 1 dequant, 2 MMA
             for (int i = 0; i < kNRv; i++) last_use[i] = 0;
-            const uint16_t all_mask = (uint16_t)((1u << p.cs) - 1u);
             for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
                 if (*abort) return false;
                 const Geo g = unit_geo(U, p);
@@ -980,10 +953,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         }
                         C++;
                     }
-                    // B slice: the unit's rows only (one 128-row box, or 64 and/or 32-row boxes).
-                    // Each CTA expects the bytes on its own barrier once its previous use of the stage
-                    // is released; the cluster leader issues the copy, multicast to every CTA, once
-                    // every CTA has released the stage.
+                    // B slice: the unit's rows only (one 128-row box, or 64 and/or 32-row boxes),
+                    // once the stage's previous slice is released.
                     if (!do_b) continue;
                     const int sb = GB % kNB;
                     if (GB >= kNB && !thread_wait(&ctl->bempty[sb], ((GB / kNB) - 1) & 1, abort, p.status, 11, GB))
@@ -994,17 +965,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     const int r64 = (r128 == 0 && U.n > 32) ? 64 : 0;
                     const int r32 = (r128 == 0 && U.n - r64 > 0) ? 32 : 0;
                     mbar_arrive_expect_tx(&ctl->bfull[sb], (uint32_t)(r128 + r64 + r32) * 128u);
-                    if (rank == 0) {
-                        if (p.cs > 1) {
-                            if (r128) tma_load_2d_mc(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb], all_mask);
-                            if (r64) tma_load_2d_mc(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb], all_mask);
-                            if (r32) tma_load_2d_mc(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb], all_mask);
-                        } else {
-                            if (r128) tma_load_2d(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb]);
-                            if (r64) tma_load_2d(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb]);
-                            if (r32) tma_load_2d(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb]);
-                        }
-                    }
+                    if (r128) tma_load_2d(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb]);
+                    if (r64) tma_load_2d(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb]);
+                    if (r32) tma_load_2d(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb]);
                     GB++;
                 }
                 return true;
@@ -1019,15 +982,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     (void)mbar_wait(&ctl->bfull[c % kNB], (c / kNB) & 1, 1000000ull);
                 }
             }
-            // The peers' releases of the last B stages arrive here asynchronously (remote
-            // mbarrier arrivals): the leader must not leave while one is still on its way, or it
-            // lands in the shared memory of whatever runs next on this SM.
-            if (do_b && rank == 0 && p.cs > 1) {
-                for (int i = 1; i <= kNB && i <= GB; i++) {
-                    const int c = GB - i;
-                    (void)mbar_wait(&ctl->bempty[c % kNB], (c / kNB) & 1, *abort ? 1000000ull : kWaitNs);
-                }
-            }
         }
     }
 
@@ -1037,16 +991,6 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         tc::fence_after();
         tc::tmem_dealloc(tbase, 512);
     }
-    // No CTA leaves while a copy into its shared memory may still be in flight.  Without a
-    // time-out every CTA has consumed every slice sent to it.  After one, slices the leader
-    // issued may be unconsumed: once no CTA issues any more (first barrier), a CTA that gave
-    // up lets copies in flight land (they take microseconds) before anyone exits.
-    cluster_sync();
-    if (*abort && threadIdx.x == 0) {
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 50000ull) __nanosleep(1000);
-    }
-    cluster_sync();
 }
 
 // ================================================================== host side
@@ -1129,38 +1073,11 @@ size_t expert_smem(int E) {
 }
 size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCtl); }
 
-// Launch one expert kernel as clusters of p.cs CTAs (the largest of 8, 4, 2, 1 dividing the
-// routed and shared tile counts that the device can co-schedule), one CTA per SM.
+// Launch one expert kernel, one CTA per SM.
 template <int NM>
 cudaError_t launch_expert(ExpertParams& p, int n_sm, int E, cudaStream_t st) {
-    const size_t smem = expert_smem<NM>(E);
-    for (int cs = kMaxCluster; cs >= 1; cs >>= 1) {
-        if (p.MT % cs || p.MTs % cs) continue;
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kExpertThreads);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = st;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        cfg.gridDim = dim3((n_sm / cs) * cs);
-        int ncl = 0;
-        if (cs > 1) {
-            if (cudaOccupancyMaxActiveClusters(&ncl, pf_expert_kernel<NM>, &cfg) != cudaSuccess) {
-                (void)cudaGetLastError();
-                continue;
-            }
-            if (ncl < 1) continue;
-            cfg.gridDim = dim3(std::min(ncl, n_sm / cs) * cs);
-        }
-        p.cs = cs;
-        return cudaLaunchKernelEx(&cfg, pf_expert_kernel<NM>, p);
-    }
-    return cudaErrorNotSupported;
+    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem<NM>(E), st>>>(p);
+    return cudaGetLastError();
 }
 
 int router_splits(int E, int T, int H, int n_sm) {

@@ -102,16 +102,6 @@ __device__ __forceinline__ void commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Arrive once on the mbarrier at `bar`'s offset in every CTA of the cluster named in
-// `cta_mask` when every MMA this thread issued so far has completed.
-__device__ __forceinline__ void commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // ------------------------------------------------------------------ TMEM <-> registers (whole warp)
 
 // 16 consecutive 32-bit columns of this thread's lane.
