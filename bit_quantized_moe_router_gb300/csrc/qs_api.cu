@@ -9,7 +9,7 @@ namespace qs {
 
 static thread_local int g_last_cuda_error = 0;
 
-static int cuda_fail(cudaError_t e) {
+int cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
     return QS_ERR_CUDA;
 }
@@ -43,6 +43,10 @@ WsLayout ws_layout(const qs_moe_shape& s, int T) {
     L.xhs = take(tf * std::max<size_t>(S, 1) * 4);
     L.xh = take(tf * k * F * 4);
     const size_t H = (size_t)s.hidden;
+    const size_t tc = std::min<size_t>(t, kClusterMaxT);
+    L.cx = take(kCxBytes);
+    L.cpd = take(tc * k * H * 4);
+    L.csdp = take(tc * H * 4);
     L.wr3 = take(3 * E * H * 2);
     L.lpart = take((size_t)kPrefillMaxKS * t * E * 4);
     L.xs = take(t * k * H * 2);
@@ -79,6 +83,34 @@ static bool shared_ok(const qs_moe_shape* s, const qs_shared_expert* sh) {
 template <class T>
 static T* ws_at(void* ws, size_t off) {
     return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// Which one-kernel decode path a call tries first.  Both give the layer within its tolerance.
+// Measured side by side on one GB300 (35B-A3B layer, 1 to 8 tokens; H=4096 layer, 1 token),
+// the persistent kernel -- whose 152 CTAs all take routed rows -- is the faster at every token
+// count, so it goes first; the cluster kernel takes the calls the persistent kernel's plan
+// does not.
+static bool prefer_cluster(const qs_moe_shape& s, int T) {
+    (void)s;
+    (void)T;
+    return false;
+}
+
+cudaError_t launch_decode_kernel(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
+                                 const WsLayout& W, cudaStream_t st, bool x_host_mapped) {
+    const bool cluster_first = prefer_cluster(s, T);
+    for (int pass = 0; pass < 2; pass++) {
+        const bool cluster = (pass == 0) == cluster_first;
+        const cudaError_t e =
+            cluster ? launch_cluster_decode(s, x, Wr, bias, experts, stride, sg, su, sd, ssig, T, out, ws, W, st,
+                                            x_host_mapped)
+                    : launch_fused_decode(s, x, Wr, bias, experts, stride, sg, su, sd, ssig, T, out, ws, W, st,
+                                          x_host_mapped);
+        if (e != cudaErrorNotSupported) return e;
+    }
+    return cudaErrorNotSupported;
 }
 
 }  // namespace qs
@@ -218,12 +250,12 @@ int qs_moe_ffn(const qs_moe_shape* shape, const void* x, const float* router_w, 
     {
         qs_moe_shape eff = *shape;
         if (!has_shared) eff.shared_ffn = 0;
-        e = launch_fused_decode(eff, x, router_w, router_bias, blocks, experts->expert_stride,
-                                has_shared ? (const uint16_t*)shared->w_gate : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_up : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_down : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, workspace, L,
-                                st);
+        e = launch_decode_kernel(eff, x, router_w, router_bias, blocks, experts->expert_stride,
+                                 has_shared ? (const uint16_t*)shared->w_gate : nullptr,
+                                 has_shared ? (const uint16_t*)shared->w_up : nullptr,
+                                 has_shared ? (const uint16_t*)shared->w_down : nullptr,
+                                 has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, workspace, L,
+                                 st, false);
         if (e == cudaSuccess) return QS_OK;
         if (e != cudaErrorNotSupported) return cuda_fail(e);
         e = launch_prefill(eff, x, router_w, router_bias, blocks, experts->expert_stride,
@@ -253,12 +285,63 @@ int qs_moe_ffn(const qs_moe_shape* shape, const void* x, const float* router_w, 
     return e == cudaSuccess ? QS_OK : cuda_fail(e);
 }
 
+// Device address of pinned (page-locked, mapped) host memory, or nullptr for any other pointer.
+static void* mapped_host(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+int qs_moe_ffn_cluster(const qs_moe_shape* shape, const void* x, const float* router_w, const float* router_bias,
+                       const qs_q2k_experts* experts, const qs_shared_expert* shared, float* out, int n_tokens,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    if (!shape_ok(shape) || !x || !router_w || !out || n_tokens < 1) return QS_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(router_w) || !experts_ok(shape, experts)) return QS_ERR_INVALID;
+    const bool has_shared = shape->shared_ffn > 0 && shared != nullptr;
+    if (has_shared && !shared_ok(shape, shared)) return QS_ERR_INVALID;
+    if (int rc = check_ws(shape, n_tokens, workspace, workspace_bytes)) return rc;
+    qs_moe_shape eff = *shape;
+    if (!has_shared) eff.shared_ffn = 0;
+    const WsLayout L = ws_layout(*shape, n_tokens);
+    const cudaError_t e = launch_cluster_decode(
+        eff, x, router_w, router_bias, static_cast<const uint8_t*>(experts->blocks), experts->expert_stride,
+        has_shared ? (const uint16_t*)shared->w_gate : nullptr, has_shared ? (const uint16_t*)shared->w_up : nullptr,
+        has_shared ? (const uint16_t*)shared->w_down : nullptr,
+        has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, workspace, L, (cudaStream_t)stream);
+    if (e == cudaErrorNotSupported) return QS_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QS_OK : cuda_fail(e);
+}
+
 int qs_moe_ffn_host(const qs_moe_shape* shape, const void* x_host, const float* router_w, const float* router_bias,
                     const qs_q2k_experts* experts, const qs_shared_expert* shared, float* out_host, int n_tokens,
                     void* workspace, size_t workspace_bytes, void* stream) {
     if (!shape_ok(shape) || !x_host || !out_host || n_tokens < 1) return QS_ERR_INVALID;
     if (!workspace || ((uintptr_t)workspace & 255u)) return QS_ERR_WORKSPACE;
     if (workspace_bytes < qs_moe_host_workspace_bytes(shape, n_tokens)) return QS_ERR_WORKSPACE;
+    {
+        // pinned x and out, a call a one-kernel decode path takes: it reads x and writes out
+        // through their mapped addresses (no copies queued around it)
+        void* xd = aligned16(x_host) ? mapped_host(x_host) : nullptr;
+        void* od = xd && aligned16(out_host) ? mapped_host(out_host) : nullptr;
+        const bool has_shared = shape->shared_ffn > 0 && shared != nullptr;
+        if (od && router_w && aligned16(router_w) && experts_ok(shape, experts) &&
+            (!has_shared || shared_ok(shape, shared))) {
+            qs_moe_shape eff = *shape;
+            if (!has_shared) eff.shared_ffn = 0;
+            const WsLayout L = ws_layout(*shape, n_tokens);
+            cudaError_t e = launch_decode_kernel(
+                eff, xd, router_w, router_bias, static_cast<const uint8_t*>(experts->blocks), experts->expert_stride,
+                has_shared ? (const uint16_t*)shared->w_gate : nullptr, has_shared ? (const uint16_t*)shared->w_up : nullptr,
+                has_shared ? (const uint16_t*)shared->w_down : nullptr,
+                has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, static_cast<float*>(od), workspace,
+                L, (cudaStream_t)stream, true);
+            if (e == cudaSuccess) return QS_OK;
+            if (e != cudaErrorNotSupported) return cuda_fail(e);
+        }
+    }
     const size_t ws_bytes = ws_layout(*shape, n_tokens).total;
     const size_t xb = host_x_bytes(*shape, n_tokens);
     uint8_t* x_dev = static_cast<uint8_t*>(workspace) + ws_bytes;
@@ -273,11 +356,27 @@ int qs_moe_ffn_host(const qs_moe_shape* shape, const void* x_host, const float* 
     return e == cudaSuccess ? QS_OK : cuda_fail(e);
 }
 
+int qs_read_routing(const qs_moe_shape* shape, int n_tokens, const void* workspace, size_t workspace_bytes,
+                    int32_t* ids_host, float* w_host, void* stream) {
+    if (!shape_ok(shape) || n_tokens < 1 || !ids_host || !w_host) return QS_ERR_INVALID;
+    if (int rc = check_ws(shape, n_tokens, const_cast<void*>(workspace), workspace_bytes)) return rc;
+    const WsLayout L = ws_layout(*shape, n_tokens);
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const size_t n = (size_t)n_tokens * shape->top_k;
+    const uint8_t* base = static_cast<const uint8_t*>(workspace);
+    e = cudaMemcpy(ids_host, base + L.ids, n * sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(w_host, base + L.pw, n * sizeof(float), cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? QS_OK : cuda_fail(e);
+}
+
 int qs_moe_ffn_launches(const qs_moe_shape* shape, int n_tokens, int has_shared) {
     if (!shape_ok(shape) || n_tokens < 1) return 0;
     qs_moe_shape eff = *shape;
     if (!has_shared) eff.shared_ffn = 0;
     cudaError_t e;
+    if (cluster_decode_supported(eff, n_tokens, &e)) return 1;
+    if (e != cudaSuccess) return -(int)e;
     if (fused_decode_supported(eff, n_tokens, &e)) return 1;
     if (e != cudaSuccess) return -(int)e;
     if (prefill_shape_ok(eff)) return prefill_launches();

@@ -51,6 +51,7 @@
 #include "qs_common.cuh"
 #include "qs_internal.h"
 #include "qs_q2k.cuh"
+#include "qs_warp.cuh"
 
 #include <algorithm>
 
@@ -65,7 +66,7 @@ constexpr int kStageBytes = 21504;       // 2 x 128 Q2_K row-blocks of 84 B
 constexpr int kMaxStages = 12;
 constexpr int kMaxEnt = 128;             // T * k
 constexpr int kMaxT = kFusedMaxT;
-constexpr int kMaxCand = 512;            // top-k candidates (per-chunk survivors)
+constexpr int kMaxCand = 512;            // tokens x 32-logit chunks x min(k, 32) the plan admits
 constexpr int kMaxRD = 16;
 
 struct FusedParams {
@@ -83,9 +84,12 @@ struct FusedParams {
     float* xhs;   // [T x S] hs
     float* xh;    // [T*k x F] h
     WsHeader* hdr;
+    int32_t* rec_ids;  // [T*k] the call's routing (written by CTA 0)
+    float* rec_p;      // [T*k]
     int H, E, k, F, S, T, x_dtype;
     int RR, RS, R, RD;  // rows per router, shared gate/up, routed gate/up and down tile
     int nstages;
+    int x_sys;  // x is host memory reached through its mapped address: the consumer warps load it
     int sg_direct;  // group B reads the shared gate/up rows from global memory (no shared tiles in the ring)
     // byte offsets inside the data region that follows FusedCtl
     int off_xq, off_sig, off_hsf, off_hq, off_pbuf, off_stages;
@@ -111,7 +115,6 @@ struct alignas(16) FusedCtl {
     uint64_t target;  // this call's target of every exchange counter
     int ids[kMaxEnt];
     float p[kMaxEnt];
-    float lsel[kMaxEnt];
     int ent_sorted[kMaxEnt];     // entries t*k+slot sorted by (expert, entry)
     int es[kMaxEnt];             // expert of ent_sorted[i]
     int es_tok[kMaxEnt];         // token of ent_sorted[i]
@@ -123,8 +126,6 @@ struct alignas(16) FusedCtl {
     float xscale[kMaxT];
     float hscale[kMaxEnt];
     float red[2 * kGT];
-    float cand_v[kMaxCand];
-    int cand_i[kMaxCand];
 };
 
 __device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGT) : "memory"); }
@@ -140,42 +141,6 @@ __device__ __forceinline__ int group_count(int id, bool pred) {
         : "r"(id), "r"((int)pred), "n"(kGT)
         : "memory");
     return r;
-}
-
-__device__ __forceinline__ int vload(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
-__device__ __forceinline__ void vstore(int* p, int v) { *reinterpret_cast<volatile int*>(p) = v; }
-
-// Relaxed gpu-scope loads of exchanged data: served by L2, never by a stale L1 line.
-__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
-    float v;
-    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ float4 ld_relaxed_f32x4(const float* p) {
-    float4 v;
-    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
-}
-
-// 64-bit exchange counters (gpu scope).
-__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
-    uint64_t v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void red_release_add_u64(uint64_t* p, uint64_t v) {
-    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ void red_relaxed_add_u64(uint64_t* p, uint64_t v) {
-    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // One thread: wait with acquire loads until the exchange counter *c reaches `target`.
@@ -354,9 +319,9 @@ __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
     {
         const uint32_t xb = (uint32_t)P.T * P.H * (P.x_dtype == QS_BF16 ? 2 : 4);
         const uint32_t sb = P.S > 0 ? (uint32_t)P.H * 2 : 0u;
-        if (lane == 0) mbar_arrive_expect_tx(&C.xbar, xb + sb);
+        if (lane == 0) mbar_arrive_expect_tx(&C.xbar, (P.x_sys ? 0u : xb) + sb);
         __syncwarp();
-        if (lane == 0) bulk_g2s(data, P.x, xb, &C.xbar);
+        if (lane == 0 && !P.x_sys) bulk_g2s(data, P.x, xb, &C.xbar);
         if (lane == 1 && sb) bulk_g2s(data + P.off_sig, P.ssig, sb, &C.xbar);
     }
     // router rows, then shared gate/up rows (unless group B reads those from global memory)
@@ -389,74 +354,6 @@ done:
 }
 
 // ------------------------------------------------------------------ warp-level arithmetic
-
-__device__ __forceinline__ void load8(const uint8_t* p, bool f32, float* v) {
-    if (f32) {
-        const float4 a = reinterpret_cast<const float4*>(p)[0];
-        const float4 b = reinterpret_cast<const float4*>(p)[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
-        const uint4 w = *reinterpret_cast<const uint4*>(p);
-        v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
-        v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
-        v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
-        v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
-    }
-}
-
-// One warp: dot products of one dense row (K elements, fp32 or bf16, shared
-// memory) with T activation rows (fp32 or bf16, shared memory), lane-strided by
-// 8 elements, then summed over the warp.  Every lane gets acc[t].
-template <int MAXT>
-__device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int K, const uint8_t* act, bool a_f32,
-                                               int T, float* acc) {
-    const int lane = threadIdx.x & 31;
-    const int wsz = w_f32 ? 4 : 2, asz = a_f32 ? 4 : 2;
-#pragma unroll
-    for (int t = 0; t < MAXT; t++) acc[t] = 0.0f;
-#pragma unroll 4
-    for (int i = lane * 8; i < K; i += 256) {  // unrolled: rows read from global memory keep loads in flight
-        float wv[8];
-        load8(w + (size_t)i * wsz, w_f32, wv);
-#pragma unroll
-        for (int t = 0; t < MAXT; t++) {
-            if (t < T) {
-                float av[8];
-                load8(act + ((size_t)t * K + i) * asz, a_f32, av);
-                float s = acc[t];
-#pragma unroll
-                for (int q = 0; q < 8; q++) s = fmaf(wv[q], av[q], s);
-                acc[t] = s;
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < MAXT; t++)
-        if (t < T) acc[t] = warp_sum(acc[t]);
-}
-
-// key order of the top-k: larger logit first, then the lower expert id.  Evaluated without
-// short-circuit so that it compiles to predicate logic, not to branches.
-__device__ __forceinline__ bool key_before(float v, int i, float ov, int oi) { return (v > ov) | ((v == ov) & (i < oi)); }
-
-// Sort 32 (value, index) pairs held one per lane into key order (bitonic network).
-__device__ __forceinline__ void warp_sort32(float& v, int& i) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, v, stride);
-            const int oi = __shfl_xor_sync(0xffffffffu, i, stride);
-            const bool first = (lane & size) == 0 || size == 32;  // this block ends up in key order
-            const bool lower = (lane & stride) == 0;
-            const bool take = (lower == first) != key_before(v, i, ov, oi);
-            v = take ? ov : v;
-            i = take ? oi : i;
-        }
-    }
-}
 
 // ------------------------------------------------------------------ the kernel
 
@@ -514,6 +411,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         if (tid == 0) C.target = (ld_relaxed_u64(ctr_exit) / gridDim.x + 1) * gridDim.x;
         const Plan L = make_plan(P);
         const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
+        if (P.x_sys) {  // x from mapped host memory: every load in flight, then the stores
+            const int nv = P.T * P.H * (x_f32 ? 4 : 2) / 16;
+            const uint4* src = static_cast<const uint4*>(P.x);
+            uint4* dst = reinterpret_cast<uint4*>(data);
+#pragma unroll 1
+            for (int i0 = tid; i0 < nv; i0 += 4 * kCT) {
+                uint4 v[4];
+#pragma unroll
+                for (int z = 0; z < 4; z++)
+                    if (i0 + z * kCT < nv) v[z] = __ldcv(src + i0 + z * kCT);
+#pragma unroll
+                for (int z = 0; z < 4; z++)
+                    if (i0 + z * kCT < nv) dst[i0 + z * kCT] = v[z];
+            }
+            asm volatile("bar.sync 4, %0;" ::"n"(kCT) : "memory");  // every consumer warp
+        }
         bool ok = warp_wait_bar(C, &C.xbar, 0);
         if (!ok) fail(C, status);
 
@@ -548,64 +461,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 ok = group_count(2, !got) == 0;
             }
             if (ok) {
-                // per 32-logit chunk: sort, keep the first k as candidates
-                const int chunks = (E + 31) / 32;
-                const int kc = min(k, 32);
-                const int nq = T * chunks;
-                // a warp's chunks one after another; each chunk's logits are loaded while the
-                // previous chunk is sorted
-                auto chunk_logit = [&](int q) {
-                    const int e = (q % chunks) * 32 + lane;
-                    return e < E ? ld_relaxed_f32(P.xlog + (size_t)(q / chunks) * E + e) : -INFINITY;
-                };
-                float vnext = gwarp < nq ? chunk_logit(gwarp) : -INFINITY;
-#pragma unroll 1
-                for (int q = gwarp; q < nq; q += kGW) {
-                    const int e = (q % chunks) * 32 + lane;
-                    float v = vnext;
-                    if (q + kGW < nq) vnext = chunk_logit(q + kGW);
-                    if (v != v) v = -INFINITY;  // a NaN logit ranks last
-                    int i = e < E ? e : 0x7fffffff;
-                    warp_sort32(v, i);
-                    if (lane < kc) {
-                        C.cand_v[q * kc + lane] = v;
-                        C.cand_i[q * kc + lane] = i;
-                    }
-                }
-                group_sync(2);
-                // rank among the token's candidates: rank < k is selected.  Four adjacent lanes
-                // share a candidate, each counting a quarter of the others.
-                const int nc = chunks * kc;
-                const int n4 = T * nc * 4;
-#pragma unroll 1
-                for (int q4 = gtid; q4 < (n4 + 31) / 32 * 32; q4 += kGT) {
-                    const bool live = q4 < n4;
-                    const int q = live ? q4 >> 2 : 0, part = q4 & 3;
-                    const int t = q / nc;
-                    const float v = C.cand_v[q];
-                    const int i = C.cand_i[q];
-                    int rank = 0;
-#pragma unroll 4
-                    for (int j = part; j < nc; j += 4) rank += key_before(C.cand_v[t * nc + j], C.cand_i[t * nc + j], v, i);
-                    rank += __shfl_xor_sync(0xffffffffu, rank, 1);
-                    rank += __shfl_xor_sync(0xffffffffu, rank, 2);
-                    if (live && part == 0 && rank < k && i < E) {
-                        C.ids[t * k + rank] = i;
-                        C.lsel[t * k + rank] = v;
-                    }
-                }
-                group_sync(2);
-                // softmax over the selected logits (one warp per token)
+                // top-k of each token's logits and the softmax over the k (one warp per token)
 #pragma unroll 1
                 for (int t = gwarp; t < T; t += kGW) {
-                    const float l0 = C.lsel[t * k];
-                    float ex = 0.0f;
-#pragma unroll 1
-                    for (int j = lane; j < k; j += 32) ex += expf(C.lsel[t * k + j] - l0);
-                    const float den = warp_sum(ex);
-#pragma unroll 1
-                    for (int j = lane; j < k; j += 32) C.p[t * k + j] = expf(C.lsel[t * k + j] - l0) / den;
+                    int id;
+                    float w;
+                    if (E <= 256) warp_topk<8>(P.xlog + (size_t)t * E, E, k, id, w);
+                    else warp_topk_stream(P.xlog + (size_t)t * E, E, k, id, w);
+                    if (lane < k) {
+                        C.ids[t * k + lane] = id;
+                        C.p[t * k + lane] = w;
+                    }
                 }
+                group_sync(2);
                 // order the entries by (expert, entry)
 #pragma unroll 1
                 for (int i = gtid; i < n_ent; i += kGT) {
@@ -643,6 +511,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 8
                     for (int j = 0; j < gtid; j++) pos += C.es_tok[j] == t;
                     C.tok_sorted[t * k + pos] = gtid;
+                }
+                if (blockIdx.x == 0) {  // the call's routing, for the caller to read back
+                    for (int i = gtid; i < n_ent; i += kGT) {
+                        P.rec_ids[i] = C.ids[i];
+                        P.rec_p[i] = C.p[i];
+                    }
                 }
                 group_sync(2);
                 if (gtid == 0) {
@@ -1144,7 +1018,7 @@ bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err) {
 cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
-                                const WsLayout& W, cudaStream_t st) {
+                                const WsLayout& W, cudaStream_t st, bool x_host_mapped) {
     DeviceFacts* f = nullptr;
     cudaError_t e = device_facts(&f);
     if (e != cudaSuccess) return e;
@@ -1165,6 +1039,8 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.xlog = reinterpret_cast<float*>(base + W.xlog);
     p.xhs = reinterpret_cast<float*>(base + W.xhs);
     p.xh = reinterpret_cast<float*>(base + W.xh);
+    p.rec_ids = reinterpret_cast<int32_t*>(base + W.ids);
+    p.rec_p = reinterpret_cast<float*>(base + W.pw);
     p.hdr = reinterpret_cast<WsHeader*>(base + W.header);
     p.H = s.hidden;
     p.E = s.n_experts;
@@ -1179,6 +1055,7 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.RD = fp.RD;
     p.nstages = fp.nstages;
     p.sg_direct = fp.sg_direct;
+    p.x_sys = x_host_mapped ? 1 : 0;
     p.off_xq = fp.off_xq;
     p.off_sig = fp.off_sig;
     p.off_hsf = fp.off_hsf;

@@ -26,6 +26,10 @@ struct WsLayout {
     size_t xlog = 0;     // [Tf x E]
     size_t xhs = 0;      // [Tf x S]
     size_t xh = 0;       // [Tf*k x F]     (Tf = min(T, kFusedMaxT))
+    // cluster decode kernel: its counters, per-entry routed down products, shared down products
+    size_t cx = 0;       // kCxBytes of 64-bit counters, one per 32-byte sector
+    size_t cpd = 0;      // f32 [Tc*k x H]  (Tc = min(T, kClusterMaxT))
+    size_t csdp = 0;     // f32 [Tc x H]
     // tensor-core (prefill) path
     size_t wr3 = 0;      // bf16 [3 x E x H]  router weights as three bf16 planes
     size_t lpart = 0;    // f32 [kPrefillMaxKS x T x E] partial logits
@@ -39,8 +43,14 @@ struct WsLayout {
 constexpr int kRouteTok = 8;    // tokens per router CTA chunk
 constexpr int kFusedMaxT = 16;  // largest token count the persistent decode kernel takes
 constexpr int kPrefillMaxKS = 4;  // largest split of H in the tensor-core router
+constexpr int kClusterCtas = 8;   // CTAs per thread-block cluster of the cluster decode kernel
+constexpr int kClusterMaxT = 8;   // largest token count the cluster decode kernel takes
+constexpr int kCxBytes = 512;     // counter region of the cluster decode kernel
 
 WsLayout ws_layout(const qs_moe_shape& s, int max_tokens);
+
+// Record e as the calling thread's last CUDA failure (qs_last_cuda_error) and return QS_ERR_CUDA.
+int cuda_fail(cudaError_t e);
 
 // Decode-path launchers (qs_decode.cu).  All return the launch's cudaError_t.
 cudaError_t launch_route(const qs_moe_shape& s, const void* x, const float* W, const float* bias, int T,
@@ -71,12 +81,31 @@ cudaError_t launch_steer_rows(float* y, const float* d, float scale, int T, int 
 
 // Persistent single-kernel decode path (qs_fused.cu).  cudaErrorNotSupported
 // when the shape or token count is outside its plan; the caller then runs the
-// per-step kernels.  sg == nullptr means no shared expert.
+// per-step kernels.  sg == nullptr means no shared expert.  x_host_mapped: x and out are
+// pinned host memory given by their device-mapped addresses (x read with plain loads).
 cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
-                                const WsLayout& W, cudaStream_t st);
+                                const WsLayout& W, cudaStream_t st, bool x_host_mapped = false);
 bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err);
+
+// Decode path of thread-block clusters (qs_cluster.cu): one kernel; a cluster of
+// kClusterCtas CTAs owns whole routed experts and shares h through distributed shared
+// memory.  cudaErrorNotSupported when the shape or token count is outside its plan.
+// x_host_mapped: x (and out) are pinned host memory given by their device-mapped
+// addresses; the kernel reads x with plain loads instead of a bulk copy.
+cudaError_t launch_cluster_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                                  const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                                  const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
+                                  const WsLayout& W, cudaStream_t st, bool x_host_mapped = false);
+bool cluster_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err);
+
+// The one-kernel decode paths in qs_moe_ffn's order of preference for this token count
+// (qs_api.cu): the first that takes the call is launched; cudaErrorNotSupported if neither.
+cudaError_t launch_decode_kernel(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
+                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
+                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
+                                 const WsLayout& W, cudaStream_t st, bool x_host_mapped);
 
 // Tensor-core path for many tokens (qs_prefill.cu): prefill_launches() launches.  Needs bf16
 // x and Q2_K row layouts it can stage (see prefill_shape_ok).

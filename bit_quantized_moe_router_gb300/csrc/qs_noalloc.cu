@@ -8,12 +8,19 @@
 // scratch kept in a fixed array inside this library instead: the caller passes
 // inputs and outputs only.
 //
-// The scratch is the persistent decode kernel's exchange area (status word,
-// call epoch, exit counter, tagged logits / hs / h).  It is one array shared by
-// every call on a device and it keeps the last call's contents; the epoch in it
-// is what lets a call tell its own exchanged words from the previous call's.
-// Calls that overlap on the GPU (different streams, no ordering between them)
-// race on it.
+// The scratch is the exchange area of the decode kernels (the one-kernel paths
+// of qs_moe_ffn; the same one runs here for the same call): the 256-byte header
+// (sticky status word and the counters of the persistent kernel), the counter
+// region of the cluster kernel, the routing record (ids, weights), and the
+// exchanged fp32 arrays -- logits [T x E], the shared expert's hs [T x S], the
+// routed h [T*k x F] (persistent kernel), the per-entry down products
+// [T*k x H] and the shared down products [T x H] (cluster kernel) -- the same
+// regions a workspace holds.  The counters are never reset: every call adds a
+// fixed amount to each of them, and a call's targets follow from its exit
+// counter, read once the previous grid has completed.  So the array needs
+// zeroing only once, at set-up.  It is one array shared by every call on a
+// device and it keeps the last call's contents; calls that overlap on the GPU
+// (different streams, no ordering between them) race on it.
 #include "qs_common.cuh"
 #include "qs_internal.h"
 
@@ -33,30 +40,43 @@ void* g_scratch_ptr[kMaxDev] = {};
 
 inline size_t up256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Exchange-area layout for T tokens: header, then the three tagged regions.
+// Exchange-area layout for T tokens: header, counters, routing record, exchanged fp32 regions.
 qs::WsLayout noalloc_layout(const qs_moe_shape& s, int T) {
     qs::WsLayout L;
     size_t o = 0;
-    L.header = o;
-    o += up256(qs::kHeaderBytes);
-    L.xlog = o;
-    o += up256((size_t)T * s.n_experts * 8);
-    L.xhs = o;
-    o += up256((size_t)T * (s.shared_ffn > 0 ? s.shared_ffn : 1) * 8);
-    L.xh = o;
-    o += up256((size_t)T * s.top_k * s.expert_ffn * 8);
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += up256(bytes);
+        return at;
+    };
+    const size_t tk = (size_t)T * s.top_k;
+    L.header = take(qs::kHeaderBytes);
+    L.cx = take(qs::kCxBytes);
+    L.ids = take(tk * 4);
+    L.pw = take(tk * 4);
+    L.xlog = take((size_t)T * s.n_experts * 4);
+    L.xhs = take((size_t)T * (s.shared_ffn > 0 ? s.shared_ffn : 1) * 4);
+    L.xh = take(tk * s.expert_ffn * 4);
+    L.cpd = take(tk * s.hidden * 4);
+    L.csdp = take((size_t)T * s.hidden * 4);
     L.total = o;
     return L;
 }
 
+// The current device's index, checked against the table below.
+cudaError_t current_device(int* dev) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    return (*dev < 0 || *dev >= kMaxDev) ? cudaErrorInvalidDevice : cudaSuccess;
+}
+
 // Device address of the scratch array on the current device.  The first call on
-// a device looks the address up and zeroes the array (so the status word, exit
-// counter and epoch start at 0); later calls reuse it.
+// a device looks the address up and zeroes the array (so the status word, the
+// exchange counters and the exit counter start at 0); later calls reuse it.
 cudaError_t scratch_for_current_device(void** out, cudaStream_t st) {
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_scratch_ptr[dev] == nullptr) {
         void* p = nullptr;
@@ -93,16 +113,46 @@ extern "C" int qs_moe_ffn_noalloc(const qs_moe_shape* shape, const void* x, cons
     if (n_tokens > qs::kFusedMaxT) return QS_ERR_UNSUPPORTED;
     const qs::WsLayout L = noalloc_layout(eff, n_tokens);
     if (L.total > kNoAllocScratchBytes) return QS_ERR_WORKSPACE;
+    // the kernel qs_moe_ffn would run for this call: one of the two one-kernel decode paths
     cudaError_t e;
-    if (!qs::fused_decode_supported(eff, n_tokens, &e)) return e == cudaSuccess ? QS_ERR_UNSUPPORTED : QS_ERR_CUDA;
+    const bool cluster = qs::cluster_decode_supported(eff, n_tokens, &e);
+    if (e != cudaSuccess) return qs::cuda_fail(e);
+    if (!cluster && !qs::fused_decode_supported(eff, n_tokens, &e))
+        return e == cudaSuccess ? QS_ERR_UNSUPPORTED : qs::cuda_fail(e);
+    if (e != cudaSuccess) return qs::cuda_fail(e);
     void* scratch = nullptr;
     e = scratch_for_current_device(&scratch, (cudaStream_t)stream);
-    if (e != cudaSuccess) return QS_ERR_CUDA;
-    e = qs::launch_fused_decode(eff, x, router_w, router_bias, static_cast<const uint8_t*>(experts->blocks),
-                                experts->expert_stride, has_shared ? (const uint16_t*)shared->w_gate : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_up : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_down : nullptr,
-                                has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, scratch, L,
-                                (cudaStream_t)stream);
-    return e == cudaSuccess ? QS_OK : QS_ERR_CUDA;
+    if (e != cudaSuccess) return qs::cuda_fail(e);
+    const uint8_t* blocks = static_cast<const uint8_t*>(experts->blocks);
+    const uint16_t* wg = has_shared ? (const uint16_t*)shared->w_gate : nullptr;
+    const uint16_t* wu = has_shared ? (const uint16_t*)shared->w_up : nullptr;
+    const uint16_t* wd = has_shared ? (const uint16_t*)shared->w_down : nullptr;
+    const uint16_t* wsig = has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr;
+    e = qs::launch_decode_kernel(eff, x, router_w, router_bias, blocks, experts->expert_stride, wg, wu, wd, wsig,
+                                 n_tokens, out, scratch, L, (cudaStream_t)stream, false);
+    if (e == cudaErrorNotSupported) return QS_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? QS_OK : qs::cuda_fail(e);
+}
+
+extern "C" int qs_noalloc_read_device_status(void* stream) {
+    int dev = 0;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return qs::cuda_fail(e);
+    void* p = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        p = g_scratch_ptr[dev];
+    }
+    e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return qs::cuda_fail(e);
+    if (p == nullptr) return QS_OK;  // no call has run on this device
+    uint32_t st = 0;
+    e = cudaMemcpy(&st, p, sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return qs::cuda_fail(e);
+    if (st != 0) {  // clear the status word only; the counters stay consistent across a time-out
+        const uint32_t zero = 0;
+        e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return qs::cuda_fail(e);
+    }
+    return (int)st;
 }

@@ -147,19 +147,21 @@ __device__ __forceinline__ void load_q2chunk_global(const uint8_t* blk, int u, Q
 
 // Partial dot of chunk u of a block (its words in c) with the thread's activations:
 // d * sum sc_lo*S - dmin * sum sc_hi*X (unscaled by s_x).
+// Integer sums are exact, so the four words' partial sums are formed independently (short
+// dependency chains for the scheduler) and added afterwards; the result is the same bits.
 __device__ __forceinline__ float q2k_chunk_dot(const Q2Chunk& c, int u, const XFrag& f) {
     const int sh0 = 8 * (u & 1);
     int plo = 0, phi = 0;
 #pragma unroll
     for (int j = 0; j < 4; j++) {
         const uint32_t mask = 0x03030303u << (2 * j);
-        int t = 0;
+        int tw[4];
 #pragma unroll
         for (int w = 0; w < 4; w++) {
             const uint32_t v = c.q[w] & mask;
-            t = dp2a_lo(f.v[j][w][0], v, t);
-            t = dp2a_hi(f.v[j][w][1], v, t);
+            tw[w] = dp2a_hi(f.v[j][w][1], v, dp2a_lo(f.v[j][w][0], v, 0));
         }
+        int t = (tw[0] + tw[1]) + (tw[2] + tw[3]);
         t >>= 2 * j;
         const uint32_t sc = ((j < 2 ? c.sca : c.scb) >> (sh0 + 16 * (j & 1))) & 0xffu;
         plo += (int)(sc & 15u) * t;

@@ -10,6 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -23,7 +24,7 @@ EXPORTS = (
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
     "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
     "qs_moe_ffn_noalloc", "qs_steer_rows", "qs_moe_ffn_q4k", "qs_q4k_quantize", "qs_moe_host_workspace_bytes",
-    "qs_moe_ffn_host",
+    "qs_moe_ffn_host", "qs_noalloc_read_device_status", "qs_read_routing", "qs_moe_ffn_cluster",
 )
 
 
@@ -86,8 +87,12 @@ def load(build_if_missing: bool = True):
     L.qs_q2k_down_combine.argtypes = [SP, EP, P, P, P, i32, P, i32, P]
     L.qs_shared_expert_ffn.argtypes = [SP, P, HP, i32, P, i32, P, sz, P]
     L.qs_moe_ffn.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
+    L.qs_moe_ffn_cluster.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
     L.qs_moe_ffn_launches.argtypes = [SP, i32, i32]
     L.qs_moe_ffn_noalloc.argtypes = [SP, P, P, P, EP, HP, P, i32, P]
+    L.qs_noalloc_read_device_status.restype = i32
+    L.qs_read_routing.argtypes = [SP, i32, P, sz, P, P, P]
+    L.qs_noalloc_read_device_status.argtypes = [P]
     L.qs_q2k_quantize.argtypes = [P, i64, i64, P, P]
     L.qs_test_wait_timeout.argtypes = [P, sz, i32, P]
     L.qs_steer_rows.argtypes = [P, P, ctypes.c_float, i32, i32, P]
@@ -221,12 +226,37 @@ def qs_moe_ffn(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared,
                              _stream(stream)), "qs_moe_ffn")
 
 
+def qs_moe_ffn_cluster(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens, workspace,
+                       stream=None):
+    """The whole layer through the cluster decode kernel alone (QsError QS_ERR_UNSUPPORTED outside its plan)."""
+    _check(load().qs_moe_ffn_cluster(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
+                                     ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
+                                     n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "qs_moe_ffn_cluster")
+
+
 def qs_moe_ffn_noalloc(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens,
                        stream=None):
     """The whole layer with its scratch in a fixed array inside the library (no workspace argument)."""
     _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                                      ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
                                      _dptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
+
+
+def qs_read_routing(shape, n_tokens, workspace, stream=None):
+    """(ids int32 [n_tokens, k], weights fp32 [n_tokens, k]) the last qs_moe_ffn call on workspace used."""
+    k = shape.top_k
+    ids = np.zeros((n_tokens, k), np.int32)
+    w = np.zeros((n_tokens, k), np.float32)
+    _check(load().qs_read_routing(ctypes.byref(shape), n_tokens, _dptr(workspace),
+                                  workspace.numel() * workspace.element_size(), ids.ctypes.data, w.ctypes.data,
+                                  _stream(stream)), "qs_read_routing")
+    return ids, w
+
+
+def qs_noalloc_read_device_status(stream=None) -> int:
+    """Sticky device status of the qs_moe_ffn_noalloc array on the current device, cleared by the read."""
+    return load().qs_noalloc_read_device_status(_stream(stream))
 
 
 def qs_steer_rows(out, direction, scale, n_tokens, stream=None):

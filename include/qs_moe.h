@@ -185,6 +185,7 @@ int qs_shared_expert_ffn(const qs_moe_shape *shape, const void *x, const qs_shar
  *    kernel in the stream finishes, prefetching weights into L2 meanwhile, and
  *    waits for that kernel before it reads x or writes anything.  The result
  *    does not depend on how tokens are batched;
+ *  - else, up to 8 tokens, the cluster decode kernel (qs_moe_ffn_cluster);
  *  - otherwise, with bf16 x (and Q2_K rows it can stage: hidden a multiple of
  *    1024 or equal to 256; expert_ffn a multiple of 1024 or at most 768): the
  *    tensor-core path -- router on the tensor cores as three exact bf16 planes
@@ -196,6 +197,25 @@ int qs_shared_expert_ffn(const qs_moe_shape *shape, const void *x, const qs_shar
 int qs_moe_ffn(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
                const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                void *workspace, size_t workspace_bytes, void *stream);
+
+/* The whole layer through the cluster decode kernel alone (no other path):
+ * the grid is thread-block clusters of 8 CTAs, one CTA per SM; a cluster owns
+ * whole routed experts -- its 8 CTAs each compute 1/8 of an expert's gate/up
+ * rows, share the slices of h through distributed shared memory, and each
+ * forms the expert's down product over 1/8 of the output rows -- and a
+ * per-slice ticket lets the CTA that completes a slice add the experts' down
+ * products and the shared expert's in slot order.  Same arguments, result
+ * (within the layer's tolerance), workspace and error behaviour as
+ * qs_moe_ffn, for up to 8 tokens with top_k * n_tokens <= 64 and
+ * power-of-two block counts per row; otherwise QS_ERR_UNSUPPORTED.
+ * qs_moe_ffn does not pick it first: measured on GB300 it is slower than the
+ * persistent kernel at every token count tried, because with 15 clusters of 8
+ * only the clusters that own an active expert carry the routed rows (64 of 120
+ * SMs at one token).  Needs every cluster resident at once, like the
+ * persistent kernel (a wait bound ends the call in QS_ERR_TIMEOUT otherwise). */
+int qs_moe_ffn_cluster(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
+                       const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
+                       void *workspace, size_t workspace_bytes, void *stream);
 
 /* The whole layer without a workspace argument (the pages have no
  * counterpart; this is a convenience of this library).  For callers that
@@ -210,11 +230,20 @@ int qs_moe_ffn(const qs_moe_shape *shape, const void *x, const float *router_w, 
  * call on a device looks the array up and zeroes it, synchronising `stream`,
  * so make that first call before any stream capture.  Every call on a device
  * shares the array and it keeps the last call's contents; calls that overlap
- * on the GPU race on it.  Device-side time-outs are recorded in the array's
- * status word, which this entry point does not report. */
+ * on the GPU race on it.  A device-side time-out (the persistent kernel waits
+ * for every CTA, so other work holding SMs past the wait bound ends it early)
+ * leaves out's rows incomplete and is recorded in the array's sticky status
+ * word: read it with qs_noalloc_read_device_status after the call. */
 int qs_moe_ffn_noalloc(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
                        const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                        void *stream);
+
+/* Synchronise `stream`, then return the sticky device status of the current
+ * device's qs_moe_ffn_noalloc array (QS_OK, or QS_ERR_TIMEOUT if a call since
+ * the last read ran out of a device-side wait and its output is not valid) and
+ * clear it.  QS_OK if no qs_moe_ffn_noalloc call has run on this device;
+ * QS_ERR_CUDA if the sync or the 4-byte copies fail.  Allocates nothing. */
+int qs_noalloc_read_device_status(void *stream);
 
 /* The whole layer with Q4_K routed experts: the same routing, grouping and
  * gated bf16 shared expert as qs_moe_ffn, the routed gate/up (SwiGLU) and down
@@ -252,8 +281,12 @@ int qs_steer_rows(float *out, const float *direction, float scale, int n_tokens,
 /* The whole layer with x and out in host memory: queues on `stream` a copy of
  * x (host, [n_tokens x H], x_dtype) into the workspace, the qs_moe_ffn call
  * and a copy of the result into out_host (host fp32 [n_tokens x H]), then
- * returns; synchronise the stream before reading out_host.  Host buffers
- * should be pinned (page-locked) for the copies to be asynchronous.  Weights,
+ * returns; synchronise the stream before reading out_host.  When both host
+ * buffers are pinned (page-locked, so mapped into the device's address space;
+ * 16-byte aligned) and the call is one the cluster decode kernel takes, that
+ * kernel reads x and writes out through their mapped addresses instead, with
+ * no copies queued.  Host buffers should be pinned for the copies to be
+ * asynchronous.  Weights,
  * shared expert and workspace are device memory as for qs_moe_ffn;
  * workspace: qs_moe_host_workspace_bytes(shape, n_tokens) bytes, 256-byte
  * aligned, initialised with qs_workspace_init (the layer's workspace first,
@@ -262,6 +295,17 @@ size_t qs_moe_host_workspace_bytes(const qs_moe_shape *shape, int max_tokens);
 int qs_moe_ffn_host(const qs_moe_shape *shape, const void *x_host, const float *router_w, const float *router_bias,
                     const qs_q2k_experts *experts, const qs_shared_expert *shared, float *out_host, int n_tokens,
                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* The routing the last qs_moe_ffn (or qs_moe_ffn_host) call on `workspace`
+ * chose, as its kernels used it: synchronise `stream`, then copy to host memory
+ * ids_host int32 [n_tokens x k] (expert ids, descending logit, ties to the lower
+ * id) and w_host fp32 [n_tokens x k] (softmax over the selected logits).
+ * n_tokens and shape must be the call's; workspace as for qs_moe_ffn.  Every
+ * implementation records it (the one-kernel paths from their first CTA, after
+ * its top-k; the others from their routing kernel).  QS_ERR_CUDA if the sync or
+ * a copy fails. */
+int qs_read_routing(const qs_moe_shape *shape, int n_tokens, const void *workspace, size_t workspace_bytes,
+                    int32_t *ids_host, float *w_host, void *stream);
 
 /* Number of kernels one qs_moe_ffn call with this shape, token count and
  * shared expert (has_shared != 0) launches on the current device: 1 for the
