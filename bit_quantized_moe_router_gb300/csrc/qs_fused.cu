@@ -57,10 +57,14 @@
 
 namespace qs {
 
-constexpr int kCW = 16;                  // consumer warps
+// 16 warps at one CTA per SM leave 128 registers per thread (a seventeenth warp would put five
+// warps on one of the SM's four schedulers and cap every thread at 96)
+constexpr int kCW = 15;                  // consumer warps
 constexpr int kCT = kCW * 32;            // consumer threads
-constexpr int kGW = 8;                   // warps per consumer group
-constexpr int kGT = kGW * 32;            // threads per consumer group
+constexpr int kGWA = 8;                  // warps of consumer group A (router rows, routing)
+constexpr int kGWB = kCW - kGWA;         // warps of consumer group B (x preparation, shared gate/up rows)
+constexpr int kGTA = kGWA * 32;
+constexpr int kGTB = kGWB * 32;
 constexpr int kFusedThreads = kCT + 32;  // + the producer warp
 constexpr int kStageBytes = 21504;       // 2 x 128 Q2_K row-blocks of 84 B
 constexpr int kMaxStages = 12;
@@ -125,12 +129,15 @@ struct alignas(16) FusedCtl {
     float gate_s[kMaxT];
     float xscale[kMaxT];
     float hscale[kMaxEnt];
-    float red[2 * kGT];
+    float red[2 * kGTB];
 };
 
-__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kGT) : "memory"); }
+// Named barriers of the consumer groups: 2 for group A, 3 for group B.
+template <int NT>
+__device__ __forceinline__ void group_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(NT) : "memory"); }
 
-// number of threads of consumer group `id` whose predicate is true (a group barrier)
+// number of threads of consumer group `id` whose predicate is true (a group barrier of NT threads)
+template <int NT>
 __device__ __forceinline__ int group_count(int id, bool pred) {
     int r;
     asm volatile(
@@ -138,7 +145,7 @@ __device__ __forceinline__ int group_count(int id, bool pred) {
         "setp.ne.u32 p, %2, 0;\n\t"
         "bar.red.popc.u32 %0, %1, %3, p;\n\t}"
         : "=r"(r)
-        : "r"(id), "r"((int)pred), "n"(kGT)
+        : "r"(id), "r"((int)pred), "n"(NT)
         : "memory");
     return r;
 }
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
     const uint8_t* sigbuf = data + P.off_sig;                                // [H] bf16
     float* hsf = reinterpret_cast<float*>(data + P.off_hsf);                 // [T x S]
     uint32_t* hqf = reinterpret_cast<uint32_t*>(data + P.off_hq);            // [T*k][F/64 chunks][36] fragments
-    float* pbuf = reinterpret_cast<float*>(data + P.off_pbuf);               // [16 warps x kMaxEnt]
+    float* pbuf = reinterpret_cast<float*>(data + P.off_pbuf);               // [consumer warps x kMaxEnt]
     uint8_t* stages = data + P.off_stages;
     const int ns = P.nstages;
 
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         // CTA publishes its logits: the exit count is an exact multiple of gridDim here
         if (tid == 0) C.target = (ld_relaxed_u64(ctr_exit) / gridDim.x + 1) * gridDim.x;
         const Plan L = make_plan(P);
-        const int gtid = tid & (kGT - 1), gwarp = warp & (kGW - 1);
+        const int gtid = warp < kGWA ? tid : tid - kGTA, gwarp = warp < kGWA ? warp : warp - kGWA;
         if (P.x_sys) {  // x from mapped host memory: every load in flight, then the stores
             const int nv = P.T * P.H * (x_f32 ? 4 : 2) / 16;
             const uint4* src = static_cast<const uint4*>(P.x);
@@ -430,10 +437,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         bool ok = warp_wait_bar(C, &C.xbar, 0);
         if (!ok) fail(C, status);
 
-        if (warp < kGW) {
+        if (warp < kGWA) {
             // ------------------------------------------------------ group A: router rows
 #pragma unroll 1
-            for (int idx = gwarp; ok && idx < L.own_rt * P.RR; idx += kGW) {
+            for (int idx = gwarp; ok && idx < L.own_rt * P.RR; idx += kGWA) {
                 const int m = idx / P.RR, r = idx % P.RR;
                 const int g = L.cta + m * L.G;
                 if (!(ok = warp_wait_tile(C, m, ns))) break;
@@ -451,19 +458,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             // ------------------------------------------------------ group A: routing
             // group-uniform outcome of the previous waits; the barrier also orders every
             // logit this group stored before the release below
-            ok = group_count(2, !ok) == 0;
+            ok = group_count<kGTA>(2, !ok) == 0;
             if (ok) {
                 bool got = true;
                 if (gtid == 0) {
                     publish(C, ctr_lg, kPubLogits);
                     got = wait_count(ctr_lg, C.target, &C.abort);
                 }
-                ok = group_count(2, !got) == 0;
+                ok = group_count<kGTA>(2, !got) == 0;
             }
             if (ok) {
                 // top-k of each token's logits and the softmax over the k (one warp per token)
 #pragma unroll 1
-                for (int t = gwarp; t < T; t += kGW) {
+                for (int t = gwarp; t < T; t += kGWA) {
                     int id;
                     float w;
                     if (E <= 256) warp_topk<8>(P.xlog + (size_t)t * E, E, k, id, w);
@@ -473,10 +480,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         C.p[t * k + lane] = w;
                     }
                 }
-                group_sync(2);
+                group_sync<kGTA>(2);
                 // order the entries by (expert, entry)
 #pragma unroll 1
-                for (int i = gtid; i < n_ent; i += kGT) {
+                for (int i = gtid; i < n_ent; i += kGTA) {
                     const int e = C.ids[i];
                     int rank = 0;
 #pragma unroll 8
@@ -488,12 +495,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     C.es[rank] = e;
                     C.es_tok[rank] = i / k;
                 }
-                group_sync(2);
+                group_sync<kGTA>(2);
                 // active experts: a run start in es[] opens a new active expert
                 const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
                 const unsigned bal = __ballot_sync(0xffffffffu, start);
                 if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
-                group_sync(2);
+                group_sync<kGTA>(2);
                 if (gtid < n_ent) {
                     int a = __popc(bal & ((2u << lane) - 1u)) - 1;
 #pragma unroll 1
@@ -513,12 +520,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     C.tok_sorted[t * k + pos] = gtid;
                 }
                 if (blockIdx.x == 0) {  // the call's routing, for the caller to read back
-                    for (int i = gtid; i < n_ent; i += kGT) {
+                    for (int i = gtid; i < n_ent; i += kGTA) {
                         P.rec_ids[i] = C.ids[i];
                         P.rec_p[i] = C.p[i];
                     }
                 }
-                group_sync(2);
+                group_sync<kGTA>(2);
                 if (gtid == 0) {
                     const int n_et = C.n_active * L.tpe;
                     C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
@@ -530,13 +537,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             }
         } else {
             // ------------------------------------------------------ group B: x scales, int16 x, gates
-            ok = group_count(3, !ok) == 0;
+            ok = group_count<kGTB>(3, !ok) == 0;
             if (ok) {
                 float mx[MAXT], gz[MAXT];
 #pragma unroll
                 for (int t = 0; t < MAXT; t++) mx[t] = gz[t] = 0.0f;
 #pragma unroll 1
-                for (int i = gtid * 8; i < H; i += kGT * 8) {
+                for (int i = gtid * 8; i < H; i += kGTB * 8) {
                     float sv[8];
                     if (S > 0) load8(sigbuf + (size_t)i * 2, false, sv);
 #pragma unroll
@@ -559,26 +566,26 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         const float z = warp_sum(gz[t]);
                         if (lane == 0) {
                             C.red[gwarp * MAXT + t] = m;
-                            C.red[kGT + gwarp * MAXT + t] = z;
+                            C.red[kGTB + gwarp * MAXT + t] = z;
                         }
                     }
                 }
-                group_sync(3);
+                group_sync<kGTB>(3);
                 if (gtid < T) {
                     float m = 0.0f, z = 0.0f;
 #pragma unroll 1
-                    for (int w = 0; w < kGW; w++) {
+                    for (int w = 0; w < kGWB; w++) {
                         m = fmaxf(m, C.red[w * MAXT + gtid]);
-                        z += C.red[kGT + w * MAXT + gtid];
+                        z += C.red[kGTB + w * MAXT + gtid];
                     }
                     C.xscale[gtid] = m;
                     C.gate_s[gtid] = sigmoid(z);
                 }
-                group_sync(3);
+                group_sync<kGTB>(3);
                 // int16 x in fragment layout; each 8-value group is one 16-byte store, the
                 // two groups of a 16-value shift group are adjacent lanes (sums via shuffle)
 #pragma unroll 1
-                for (int i0 = gtid * 8; i0 < ((T * H + 255) / 256) * 256; i0 += kGT * 8) {
+                for (int i0 = gtid * 8; i0 < ((T * H + 255) / 256) * 256; i0 += kGTB * 8) {
                     const bool live = i0 < T * H;
                     const int t = live ? i0 / H : 0, p = live ? i0 - t * H : 0;
                     const float m = C.xscale[t];
@@ -603,14 +610,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
                     }
                 }
-                group_sync(3);
+                group_sync<kGTB>(3);
                 if (gtid == 0) mbar_arrive(&C.xq_bar);
             } else {
                 fail(C, status);
             }
             // ------------------------------------------------------ group B: shared gate/up rows
 #pragma unroll 1
-            for (int idx = gwarp; ok && idx < L.own_st * P.RS; idx += kGW) {
+            for (int idx = gwarp; ok && idx < L.own_st * P.RS; idx += kGWB) {
                 const int m = idx / P.RS, r = idx % P.RS;
                 const int sq = L.own_rt + m;
                 const int j = first_owned(L.n_rt, L.G, L.cta) + m * L.G - L.n_rt;
@@ -635,7 +642,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             }
             if (!ok) fail(C, status);
             // every hs row of this CTA is stored: publish them (the barrier orders the stores)
-            if (group_count(3, !ok) == 0 && gtid == 0) {
+            if (group_count<kGTB>(3, !ok) == 0 && gtid == 0) {
                 publish(C, ctr_hs, kPubHs);
                 mbar_arrive(&C.shared_bar);
             }
@@ -651,7 +658,6 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int n_stage_tasks = (S > 0 ? 1 : 0) + n_ent;
         const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
         const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
-        bool xq_seen = false;
         // every routed gate/up row and every routed down row this CTA will read, requested into L2
         // at once, one 128-byte line per consumer thread at a time (gate/up lines first, in task order)
         {
@@ -684,51 +690,95 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             }
         }
-#pragma unroll 1
-        for (int q = warp; ok && q < q_all; q += kCW) {
-            if (q < q_et) {
-                // ---------------------------------------------- routed gate/up rows
-                if (!xq_seen) {
-                    if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
-                    xq_seen = true;
-                }
-                const int m = q / L.ept, rt = q % L.ept;
-                const int g = first_owned(L.n_ind, L.G, L.cta) + m * L.G;
-                const int idx = g - L.n_ind;
+        // ---------------------------------------------------------- routed gate/up rows
+        // Tasks q = warp, warp + kCW, ... below q_et.  A lane owns chunk c0 + i * cstep (i < nch) of
+        // row rl of the task; its chunks are one stream, loaded one item ahead of the one computed
+        // (so the next task's rows are in flight while this task is reduced and stored).  Per entry
+        // of the expert, the chunk dots are added in chunk order, then across lanes.
+        int q = warp;
+        if (ok && q < q_et) {
+            if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) fail(C, status);
+        }
+        if (ok && q < q_et) {
+            const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
+            const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
+            const int cstep = L.cpr >= 32 ? 32 : L.cpr;
+            const int nch = L.cpr / cstep;
+            const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
+            const int g0 = first_owned(L.n_ind, L.G, L.cta);
+            // first byte of this lane's gate row of task qq (the up row is F rows further)
+            auto task_row = [&](int qq) -> const uint8_t* {
+                const int m = qq / L.ept, rt = qq % L.ept;
+                const int idx = g0 + m * L.G - L.n_ind;
                 const int a = idx / L.tpe, tt = idx % L.tpe;
-                // lanes: (row within the task, chunk); long rows: each lane walks several chunks
-                const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
-                const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
-                const int cstep = L.cpr >= 32 ? 32 : L.cpr;
+                return P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw + rl) * L.rowH;
+            };
+            const int64_t up_off = (int64_t)P.F * L.rowH;
+            // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
+            const bool hoist = MAXT == 1 && nch == 1;
+            XFrag fx;
+            if (hoist) load_xfrag_f(xqf + (size_t)c0 * kFragWords, fx);
+            Q2Chunk pg, pu;  // the next item's words, in flight
+            {
+                const uint8_t* gr = task_row(q);
+                load_q2chunk_global(gr + (c0 >> 2) * kBlockBytes, c0 & 3, pg);
+                load_q2chunk_global(gr + up_off + (c0 >> 2) * kBlockBytes, c0 & 3, pu);
+            }
+#pragma unroll 1
+            for (; q < q_et; q += kCW) {
+                const int m = q / L.ept, rt = q % L.ept;
+                const int idx = g0 + m * L.G - L.n_ind;
+                const int a = idx / L.tpe, tt = idx % L.tpe;
                 const int r = rt * L.rpw + rl;
-                const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
-                // the rows come straight from global memory into registers: every warp's loads are
-                // in flight at once, instead of queueing in the SM's copy engine one tile after another
-                const uint8_t* grow = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + r) * L.rowH;
-                const uint8_t* urow = grow + (int64_t)P.F * L.rowH;
+                const int j0 = C.act_begin[a], ne = C.act_begin[a + 1] - j0;
+                float gacc[MAXT], uacc[MAXT];
+#pragma unroll
+                for (int e = 0; e < MAXT; e++) gacc[e] = uacc[e] = 0.0f;
 #pragma unroll 1
-                for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                    const int ent = C.ent_sorted[j];
-                    const int t = ent / k;
-                    float gv = 0.0f, uv = 0.0f;
-#pragma unroll 1
-                    for (int c = c0; c < L.cpr; c += cstep) {
-                        const int b = c >> 2, u = c & 3;
-                        XFrag f;
-                        load_xfrag_f(xqf + ((size_t)t * (H / 64) + c) * kFragWords, f);
-                        Q2Chunk gc, uc;
-                        load_q2chunk_global(grow + b * kBlockBytes, u, gc);
-                        load_q2chunk_global(urow + b * kBlockBytes, u, uc);
-                        gv += q2k_chunk_dot(gc, u, f);
-                        uv += q2k_chunk_dot(uc, u, f);
+                for (int i = 0; i < nch; i++) {
+                    const int c = c0 + i * cstep;
+                    const Q2Chunk gc = pg, uc = pu;
+                    // request the next item: this task's next chunk, or the next task's first
+                    if (i + 1 < nch) {
+                        const uint8_t* gr = task_row(q) + ((c + cstep) >> 2) * kBlockBytes;
+                        load_q2chunk_global(gr, (c + cstep) & 3, pg);
+                        load_q2chunk_global(gr + up_off, (c + cstep) & 3, pu);
+                    } else if (q + kCW < q_et) {
+                        const uint8_t* gr = task_row(q + kCW) + (c0 >> 2) * kBlockBytes;
+                        load_q2chunk_global(gr, c0 & 3, pg);
+                        load_q2chunk_global(gr + up_off, c0 & 3, pu);
                     }
-                    for (int o = min(L.cpr, 32) >> 1; o > 0; o >>= 1) {
-                        gv += __shfl_xor_sync(gm, gv, o);
-                        uv += __shfl_xor_sync(gm, uv, o);
+                    if (hoist) {
+                        if (ne > 0) {
+                            gacc[0] += q2k_chunk_dot(gc, c & 3, fx);
+                            uacc[0] += q2k_chunk_dot(uc, c & 3, fx);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < MAXT; e++) {
+                            if (e < ne) {
+                                const int t = C.ent_sorted[j0 + e] / k;
+                                float dg, du;
+                                q2k_chunk_dot2_f(gc, uc, c & 3, xqf + ((size_t)t * (H / 64) + c) * kFragWords, dg, du);
+                                gacc[e] += dg;
+                                uacc[e] += du;
+                            }
+                        }
                     }
-                    if (c0 == 0) {
-                        const float sx = C.xscale[t] * (1.0f / 32767.0f);
-                        P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
+                }
+#pragma unroll
+                for (int e = 0; e < MAXT; e++) {
+                    if (e < ne) {
+                        float gv = gacc[e], uv = uacc[e];
+                        for (int o = min(L.cpr, 32) >> 1; o > 0; o >>= 1) {
+                            gv += __shfl_xor_sync(gm, gv, o);
+                            uv += __shfl_xor_sync(gm, uv, o);
+                        }
+                        if (c0 == 0) {
+                            const int ent = C.ent_sorted[j0 + e];
+                            const float sx = C.xscale[ent / k] * (1.0f / 32767.0f);
+                            P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
+                        }
                     }
                 }
                 __syncwarp();  // orders the lanes' h stores before lane 0's fences below
@@ -740,132 +790,155 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         publish(C, ctr_h, kPubH);
                     }
                 }
-            } else if (q < q_et + n_stage_tasks) {
-                // ---------------------------------------------- staging of hs / of one entry's int16 h
-                const int sidx = q - q_et;
-                // the int16 h cache aliases x, w_sg and the int16 x fragments: wait until group B is
-                // done with x and w_sg; the fragments' last reader, this CTA's last routed gate/up
-                // task, ends before the CTA publishes its h, so entries are staged only after the
-                // h counter below
-                if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
-                if (!(ok = warp_wait_mbar(C, &C.shared_bar, 0))) break;
-                if (S > 0 && sidx == 0) {
-                    int got = 1;
-                    if (lane == 0) got = wait_count(ctr_hs, C.target, &C.abort);
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    __syncwarp();
-                    if (!(ok = got != 0)) break;
-#pragma unroll 4
-                    for (int i = lane * 4; i < T * S; i += 128)
-                        *reinterpret_cast<float4*>(hsf + i) = ld_relaxed_f32x4(P.xhs + i);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&C.hs_bar);
-                } else {
-                    const int ent = sidx - (S > 0 ? 1 : 0);
-                    // the first entry task to get here waits for the h counter; the others for its flag
-                    int got = 1;
-                    if (lane == 0 && atomicCAS(&C.h_poller, 0, 1) == 0) {
-                        got = wait_count(ctr_h, C.target, &C.abort);
-                        if (got) mbar_arrive(&C.h_bar);
-                    }
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!(ok = got != 0 && warp_wait_mbar(C, &C.h_bar, 0))) break;
-                    const float* hr = P.xh + (size_t)ent * F;
-                    // lane: 8 consecutive values per 256; one pass for the scale, one to quantise
-                    float m = 0.0f;
-#pragma unroll 2
-                    for (int p = lane * 8; p < F; p += 256) {
-                        const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
-                        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-                        m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-                    }
-                    m = warp_max(m);
-                    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
-                    uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
-#pragma unroll 2
-                    for (int p = lane * 8; p < F; p += 256) {
-                        const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
-                        const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                        uint32_t wq[4];
-                        int sum = 0;
-#pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            const int a0 = __float2int_rn(hv[2 * q] * inv);
-                            const int a1 = __float2int_rn(hv[2 * q + 1] * inv);
-                            wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
-                            sum += a0 + a1;
-                        }
-                        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                        int word, half;
-                        frag_pos(p, word, half);
-                        *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                        if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
-                    }
-                    if (lane == 0) C.hscale[ent] = m * (1.0f / 32767.0f);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&C.staged_bar);
-                }
-            } else {
-                // ---------------------------------------------- one down row
-                const int dq = q - q_et - n_stage_tasks;
-                const int m = dq / P.RD, r = dq % P.RD;
-                const int g = first_owned(lo_dg, L.G, L.cta) + m * L.G;
-                const int r0 = (g - lo_dg) * P.RD;
-                // the shared expert's down row is read after the routed passes: request it into L1 now
-                if (S > 0 && lane * 128 < S * 2) {
-                    const uint16_t* srow = P.sd + (size_t)(r0 + r) * S;
-                    for (int l = lane; l * 128 < S * 2; l += 32)
-                        asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
-                }
-                if (ok && S > 0) ok = warp_wait_mbar(C, &C.hs_bar, 0);
-                if (ok) ok = warp_wait_mbar(C, &C.staged_bar, 0);
-                if (!ok) break;
-                // routed experts: epp experts per pass, cpf lanes per expert row; a pass's row
-                // chunks are requested before the previous pass is computed
-                const int al = L.cpf >= 32 ? 0 : lane / L.cpf;
-                const int c0 = L.cpf >= 32 ? lane : lane % L.cpf;
-                float* pb = pbuf + warp * kMaxEnt;
-                const unsigned gm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
-                const int u = c0 & 3;
-                const uint8_t* rowbase =
-                    P.experts + 2ll * P.F * L.rowH + (int64_t)(r0 + r) * L.rowF + (c0 >> 2) * kBlockBytes;
-                Q2Chunk cur{}, nxt{};
-                if (al < na) load_q2chunk_global(rowbase + (int64_t)C.act_e[al] * P.stride, u, cur);
+            }
+        }
+        // ---------------------------------------------------------- down rows: setup
+        // This warp's down items (task, pass) form one stream, loaded two items ahead.  The first
+        // two depend only on the routing: they are requested before the staging tasks and the
+        // waits for the staged h.
+        const int al = L.cpf >= 32 ? 0 : lane / L.cpf;  // epp experts per pass, cpf lanes per expert row
+        const int dc0 = L.cpf >= 32 ? lane : lane % L.cpf;
+        const unsigned dgm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
+        const int du = dc0 & 3;
+        const int np = (na + L.epp - 1) / L.epp;
+        const int f_dg = first_owned(lo_dg, L.G, L.cta);
+        float* pb = pbuf + warp * kMaxEnt;
+        const uint8_t* dbase = P.experts + 2ll * P.F * L.rowH + (dc0 >> 2) * kBlockBytes;
+        auto drow = [&](int qq) -> int {  // output row of down task qq
+            const int dq = qq - q_et - n_stage_tasks;
+            return (f_dg + (dq / P.RD) * L.G - lo_dg) * P.RD + dq % P.RD;
+        };
+        int iq = q, ip = 0;  // next item to request
+        while (iq < q_et + n_stage_tasks) iq += kCW;
+        auto load_item = [&](Q2Chunk& dst) {
+            if (iq >= q_all) return;
+            const int row = drow(iq);
+            if (ip == 0 && S > 0 && lane * 128 < S * 2) {  // the task's shared down row, into L1
+                const uint16_t* srow = P.sd + (size_t)row * S;
+                for (int l = lane; l * 128 < S * 2; l += 32) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
+            }
+            const int a = ip * L.epp + al;
+            if (a < na) load_q2chunk_global(dbase + (int64_t)row * L.rowF + (int64_t)C.act_e[a] * P.stride, du, dst);
+            if (++ip == np) {
+                ip = 0;
+                iq += kCW;
+            }
+        };
+        Q2Chunk b0{}, b1{}, b2{};
+        if (ok) {
+            load_item(b0);
+            load_item(b1);
+        }
+        // ---------------------------------------------------------- staging of hs / of one entry's int16 h
 #pragma unroll 1
-                for (int pa = 0; pa < na; pa += L.epp) {
-                    const int a = pa + al;
-                    if (a + L.epp < na) load_q2chunk_global(rowbase + (int64_t)C.act_e[a + L.epp] * P.stride, u, nxt);
-                    if (a < na) {
-#pragma unroll 1
-                        for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                            const int ent = C.ent_sorted[j];
-                            XFrag f;
-                            load_xfrag_f(hqf + ((size_t)ent * (F / 64) + c0) * kFragWords, f);
-                            float v = q2k_chunk_dot(cur, u, f);
-                            for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(gm, v, o);
-                            if (c0 == 0) pb[j] = v * C.hscale[ent];
-                        }
-                    }
-                    cur = nxt;
-                }
-                // shared expert down row
-                float sacc[MAXT];
-                if (S > 0)
-                    warp_dense_row<MAXT>(reinterpret_cast<const uint8_t*>(P.sd + (size_t)(r0 + r) * S), false, S,
-                                         reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
+        for (; ok && q < q_et + n_stage_tasks; q += kCW) {
+            const int sidx = q - q_et;
+            // the int16 h cache aliases x, w_sg and the int16 x fragments: wait until group B is
+            // done with x and w_sg; the fragments' last reader, this CTA's last routed gate/up
+            // task, ends before the CTA publishes its h, so entries are staged only after the
+            // h counter below
+            if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) break;
+            if (!(ok = warp_wait_mbar(C, &C.shared_bar, 0))) break;
+            if (S > 0 && sidx == 0) {
+                int got = 1;
+                if (lane == 0) got = wait_count(ctr_hs, C.target, &C.abort);
+                got = __shfl_sync(0xffffffffu, got, 0);
                 __syncwarp();
+                if (!(ok = got != 0)) break;
+#pragma unroll 4
+                for (int i = lane * 4; i < T * S; i += 128)
+                    *reinterpret_cast<float4*>(hsf + i) = ld_relaxed_f32x4(P.xhs + i);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&C.hs_bar);
+            } else {
+                const int ent = sidx - (S > 0 ? 1 : 0);
+                // the first entry task to get here waits for the h counter; the others for its flag
+                int got = 1;
+                if (lane == 0 && atomicCAS(&C.h_poller, 0, 1) == 0) {
+                    got = wait_count(ctr_h, C.target, &C.abort);
+                    if (got) mbar_arrive(&C.h_bar);
+                }
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!(ok = got != 0 && warp_wait_mbar(C, &C.h_bar, 0))) break;
+                const float* hr = P.xh + (size_t)ent * F;
+                // lane: 8 consecutive values per 256; one pass for the scale, one to quantise
+                float m = 0.0f;
+#pragma unroll 2
+                for (int p = lane * 8; p < F; p += 256) {
+                    const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+                    m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
+                }
+                m = warp_max(m);
+                const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+                uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
+#pragma unroll 2
+                for (int p = lane * 8; p < F; p += 256) {
+                    const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
+                    const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                    uint32_t wq[4];
+                    int sum = 0;
 #pragma unroll
-                for (int t = 0; t < MAXT; t++) {
-                    if (t < T && lane == t) {
-                        float acc = 0.0f;
-#pragma unroll 1
-                        for (int mm = 0; mm < k; mm++) {
-                            const int j = C.tok_sorted[t * k + mm];
-                            acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
-                        }
-                        if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
-                        P.out[(size_t)t * H + r0 + r] = acc;
+                    for (int q = 0; q < 4; q++) {
+                        const int a0 = __float2int_rn(hv[2 * q] * inv);
+                        const int a1 = __float2int_rn(hv[2 * q + 1] * inv);
+                        wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
+                        sum += a0 + a1;
                     }
+                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                    int word, half;
+                    frag_pos(p, word, half);
+                    *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+                    if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
+                }
+                if (lane == 0) C.hscale[ent] = m * (1.0f / 32767.0f);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&C.staged_bar);
+            }
+        }
+        // ---------------------------------------------------------- down rows
+        if (ok && q < q_all) {
+            if (S > 0) ok = warp_wait_mbar(C, &C.hs_bar, 0);
+            if (ok) ok = warp_wait_mbar(C, &C.staged_bar, 0);
+        }
+#pragma unroll 1
+        for (; ok && q < q_all; q += kCW) {
+            const int row = drow(q);
+#pragma unroll 1
+            for (int pa = 0; pa < np; pa++) {
+                load_item(b2);
+                const int a = pa * L.epp + al;
+                if (a < na) {
+#pragma unroll 1
+                    for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
+                        const int ent = C.ent_sorted[j];
+                        XFrag f;
+                        load_xfrag_f(hqf + ((size_t)ent * (F / 64) + dc0) * kFragWords, f);
+                        float v = q2k_chunk_dot(b0, du, f);
+                        for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(dgm, v, o);
+                        if (dc0 == 0) pb[j] = v * C.hscale[ent];
+                    }
+                }
+                b0 = b1;
+                b1 = b2;
+            }
+            // shared expert down row
+            float sacc[MAXT];
+            if (S > 0)
+                warp_dense_row<MAXT>(reinterpret_cast<const uint8_t*>(P.sd + (size_t)row * S), false, S,
+                                     reinterpret_cast<const uint8_t*>(hsf), true, T, sacc);
+            __syncwarp();
+#pragma unroll
+            for (int t = 0; t < MAXT; t++) {
+                if (t < T && lane == t) {
+                    float acc = 0.0f;
+#pragma unroll 1
+                    for (int mm = 0; mm < k; mm++) {
+                        const int j = C.tok_sorted[t * k + mm];
+                        acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
+                    }
+                    if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
+                    P.out[(size_t)t * H + row] = acc;
                 }
             }
         }

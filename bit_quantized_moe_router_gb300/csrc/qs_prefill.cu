@@ -853,60 +853,71 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         });
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int GA = 0, GB = 0, C = 0, V = 0;
-            for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
-                if (*abort) return false;
-                const Geo g = unit_geo(U, p);
-                const int b = V % NAB;
-                if (V >= NAB && !thread_wait(&ctl->accempty[b], ((V / NAB) - 1) & 1, abort, p.status, 5, V)) return false;
-                tc::fence_after();
-                const int nmma = max(16, (U.n + 15) & ~15);
-                const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, 128, nmma);
-                for (int kb = 0; kb < g.KB; kb++) {
-                    const int sb = (GB + kb) % kNB;
-                    if (!thread_wait(&ctl->bfull[sb], ((GB + kb) / kNB) & 1, abort, p.status, 6, GB + kb)) return false;
-                    const uint64_t bd = tc::sdesc_sw128(smem_u32(bst + sb * kBStageBytes));
-                    if (U.shared) {
-                        const int c = C + kb, slot = c % kNRv;
-                        if (!thread_wait(&ctl->rawfull[slot], (c / kNRv) & 1, abort, p.status, 7, c)) return false;
-                        tc::fence_after();
-                        const uint32_t sa = smem_u32(raw + slot * kSlotBytes);
+        // The whole warp runs the loop (its values are warp-uniform, so the MMA operands need no
+        // per-instruction move into the uniform datapath); lane 0 issues the MMAs and commits.
+        const uint32_t tmu = __shfl_sync(0xffffffffu, tbase, 0);
+        const bool leader = lane == 0;
+        int GA = 0, GB = 0, C = 0, V = 0;
+        for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
+            if (warp_aborted(abort)) return false;
+            const Geo g = unit_geo(U, p);
+            const int b = V % NAB;
+            if (V >= NAB && !warp_wait(&ctl->accempty[b], ((V / NAB) - 1) & 1, abort, p.status, 5, V)) return false;
+            tc::fence_after();
+            const int nmma = max(16, (U.n + 15) & ~15);
+            const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, 128, nmma);
+            for (int kb = 0; kb < g.KB; kb++) {
+                const int sb = (GB + kb) % kNB;
+                if (!warp_wait(&ctl->bfull[sb], ((GB + kb) / kNB) & 1, abort, p.status, 6, GB + kb)) return false;
+                const uint64_t bd = tc::sdesc_sw128(smem_u32(bst + sb * kBStageBytes));
+                if (U.shared) {
+                    const int c = C + kb, slot = c % kNRv;
+                    if (!warp_wait(&ctl->rawfull[slot], (c / kNRv) & 1, abort, p.status, 7, c)) return false;
+                    tc::fence_after();
+                    const uint32_t sa = smem_u32(raw + slot * kSlotBytes);
+                    if (leader) {
 #pragma unroll
                         for (int mq = 0; mq < NM; mq++) {
-                            const uint32_t d = tbase + (NM == 2 ? mq * 128 : b * 128);
+                            const uint32_t d = tmu + (NM == 2 ? mq * 128 : b * 128);
                             const uint64_t ad = tc::sdesc_sw128(sa + mq * kMatStride);
 #pragma unroll
                             for (int k16 = 0; k16 < 4; k16++)
                                 tc::mma_ss_f16(d, ad + 2 * k16, bd + 2 * k16, id, (kb | k16) != 0);
                         }
                         tc::commit(&ctl->rawfree_m[slot]);
-                    } else {
-                        const int Gk = GA + kb, s = Gk % NSA;
-                        if (!thread_wait(&ctl->afull[s], (Gk / NSA) & 1, abort, p.status, 8, Gk)) return false;
-                        tc::fence_after();
+                    }
+                } else {
+                    const int Gk = GA + kb, s = Gk % NSA;
+                    if (!warp_wait(&ctl->afull[s], (Gk / NSA) & 1, abort, p.status, 8, Gk)) return false;
+                    tc::fence_after();
+                    if (leader) {
 #pragma unroll
                         for (int mq = 0; mq < NM; mq++) {
-                            const uint32_t d = tbase + (NM == 2 ? mq * 128 : b * 128);
-                            const uint32_t a = tbase + kA0 + s * 32 * NM + mq * 32;
+                            const uint32_t d = tmu + (NM == 2 ? mq * 128 : b * 128);
+                            const uint32_t a = tmu + kA0 + s * 32 * NM + mq * 32;
 #pragma unroll
                             for (int k16 = 0; k16 < 4; k16++)
                                 tc::mma_ts_f16(d, a + 8 * k16, bd + 2 * k16, id, (kb | k16) != 0);
                         }
                         tc::commit(&ctl->aempty[s]);
                     }
-                    tc::commit(&ctl->bempty[sb]);
                 }
-                tc::commit(&ctl->accfull[b]);
-                GB += g.KB;
-                C += g.nch;
-                if (!U.shared) GA += g.KB;
-                V++;
-                return true;
-            });
+                if (leader) tc::commit(&ctl->bempty[sb]);
+                __syncwarp();
+            }
+            if (leader) tc::commit(&ctl->accfull[b]);
+            __syncwarp();
+            GB += g.KB;
+            C += g.nch;
+            if (!U.shared) GA += g.KB;
+            V++;
+            return true;
+        });
+        if (leader) {
             tc::commit(&ctl->drain);  // completes once every MMA issued above has
             (void)mbar_wait(&ctl->drain, 0);
         }
+        __syncwarp();
     } else {
         // ---------------------------------------------------------- TMA: raw weights (warp 13), B slices (warp 14)
         const bool do_raw = (warp == kWarpRaw), do_b = (warp == kWarpB);

@@ -172,6 +172,46 @@ __device__ __forceinline__ float q2k_chunk_dot(const Q2Chunk& c, int u, const XF
     return __fmaf_rn(d, (float)plo, __fmul_rn(-dm, (float)phi));
 }
 
+// Partial dots of chunk u of two blocks (a, b: e.g. a gate row's and an up row's) with the
+// activations of one fragment in shared memory (kFragWords layout), read one shift group at a
+// time so that few registers are live.  Each result is the same bits as q2k_chunk_dot's.
+__device__ __forceinline__ void q2k_chunk_dot2_f(const Q2Chunk& a, const Q2Chunk& b, int u, const uint32_t* frag,
+                                                 float& da, float& db) {
+    const uint4* q = reinterpret_cast<const uint4*>(frag);
+    const uint4 xs = q[8];
+    const int xsj[4] = {(int)xs.x, (int)xs.y, (int)xs.z, (int)xs.w};
+    const int sh0 = 8 * (u & 1);
+    int alo = 0, ahi = 0, blo = 0, bhi = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const uint4 p0 = q[2 * j], p1 = q[2 * j + 1];
+        const int32_t x[4][2] = {{(int32_t)p0.x, (int32_t)p0.y}, {(int32_t)p0.z, (int32_t)p0.w},
+                                 {(int32_t)p1.x, (int32_t)p1.y}, {(int32_t)p1.z, (int32_t)p1.w}};
+        const uint32_t mask = 0x03030303u << (2 * j);
+        int ta[4], tb[4];
+#pragma unroll
+        for (int w = 0; w < 4; w++) {
+            const uint32_t va = a.q[w] & mask, vb = b.q[w] & mask;
+            ta[w] = dp2a_hi(x[w][1], va, dp2a_lo(x[w][0], va, 0));
+            tb[w] = dp2a_hi(x[w][1], vb, dp2a_lo(x[w][0], vb, 0));
+        }
+        const int sa = ((ta[0] + ta[1]) + (ta[2] + ta[3])) >> (2 * j);
+        const int sb = ((tb[0] + tb[1]) + (tb[2] + tb[3])) >> (2 * j);
+        const uint32_t sca = ((j < 2 ? a.sca : a.scb) >> (sh0 + 16 * (j & 1))) & 0xffu;
+        const uint32_t scb = ((j < 2 ? b.sca : b.scb) >> (sh0 + 16 * (j & 1))) & 0xffu;
+        alo += (int)(sca & 15u) * sa;
+        ahi += (int)(sca >> 4) * xsj[j];
+        blo += (int)(scb & 15u) * sb;
+        bhi += (int)(scb >> 4) * xsj[j];
+    }
+    const float d_a = __half2float(__ushort_as_half((unsigned short)(a.dd & 0xffffu)));
+    const float m_a = __half2float(__ushort_as_half((unsigned short)(a.dd >> 16)));
+    const float d_b = __half2float(__ushort_as_half((unsigned short)(b.dd & 0xffffu)));
+    const float m_b = __half2float(__ushort_as_half((unsigned short)(b.dd >> 16)));
+    da = __fmaf_rn(d_a, (float)alo, __fmul_rn(-m_a, (float)ahi));
+    db = __fmaf_rn(d_b, (float)blo, __fmul_rn(-m_b, (float)bhi));
+}
+
 // Partial dot of chunk u of the block at blk (shared memory, 4-byte aligned).
 __device__ __forceinline__ float q2k_chunk_dot(const uint8_t* blk, int u, const XFrag& f) {
     Q2Chunk c;

@@ -143,6 +143,20 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+def _need_rows(t, n_tokens, row_bytes, what):
+    """Reject a tensor smaller than n_tokens rows of row_bytes (a raw address is taken as given)."""
+    if t is None or isinstance(t, int):
+        return
+    have = t.numel() * t.element_size()
+    if have < n_tokens * row_bytes:
+        raise ValueError(f"{what}: {have} bytes, need {n_tokens} rows of {row_bytes} bytes")
+
+
+def _layer_io(shape, x, out, n_tokens):
+    _need_rows(x, n_tokens, shape.hidden * (2 if shape.x_dtype == QS_BF16 else 4), "x")
+    _need_rows(out, n_tokens, shape.hidden * 4, "out")
+
+
 def _check(rc: int, what: str):
     if rc != QS_OK:
         raise QsError(rc, what)
@@ -220,6 +234,7 @@ def qs_shared_expert_ffn(shape, x, shared: qs_shared_expert, n_tokens, out, work
 
 def qs_moe_ffn(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens, workspace,
                stream=None):
+    _layer_io(shape, x, out, n_tokens)
     _check(load().qs_moe_ffn(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                              ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
                              n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
@@ -229,6 +244,7 @@ def qs_moe_ffn(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared,
 def qs_moe_ffn_cluster(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens, workspace,
                        stream=None):
     """The whole layer through the cluster decode kernel alone (QsError QS_ERR_UNSUPPORTED outside its plan)."""
+    _layer_io(shape, x, out, n_tokens)
     _check(load().qs_moe_ffn_cluster(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                                      ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
                                      n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
@@ -238,6 +254,7 @@ def qs_moe_ffn_cluster(shape, x, router_w, router_bias, experts: qs_q2k_experts,
 def qs_moe_ffn_noalloc(shape, x, router_w, router_bias, experts: qs_q2k_experts, shared, out, n_tokens,
                        stream=None):
     """The whole layer with its scratch in a fixed array inside the library (no workspace argument)."""
+    _layer_io(shape, x, out, n_tokens)
     _check(load().qs_moe_ffn_noalloc(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                                      ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
                                      _dptr(out), n_tokens, _stream(stream)), "qs_moe_ffn_noalloc")
@@ -268,6 +285,7 @@ def qs_steer_rows(out, direction, scale, n_tokens, stream=None):
 def qs_moe_ffn_host(shape, x_host, router_w, router_bias, experts: qs_q2k_experts, shared, out_host, n_tokens,
                     workspace, stream=None):
     """The whole layer with x_host and out_host in (pinned) host memory; copies are queued on the stream."""
+    _layer_io(shape, x_host, out_host, n_tokens)
     _check(load().qs_moe_ffn_host(ctypes.byref(shape), _hptr(x_host), _dptr(router_w), _dptr(router_bias),
                                   ctypes.byref(experts), None if shared is None else ctypes.byref(shared),
                                   _hptr(out_host), n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),
@@ -301,6 +319,7 @@ def qs_q4k_quantize(w, out, stream=None):
 def qs_moe_ffn_q4k(shape, x, router_w, router_bias, experts: qs_q4k_experts, shared, out, n_tokens, workspace,
                    stream=None):
     """The whole layer with Q4_K routed experts (same arguments as qs_moe_ffn)."""
+    _layer_io(shape, x, out, n_tokens)
     _check(load().qs_moe_ffn_q4k(ctypes.byref(shape), _dptr(x), _dptr(router_w), _dptr(router_bias),
                                  ctypes.byref(experts), None if shared is None else ctypes.byref(shared), _dptr(out),
                                  n_tokens, _dptr(workspace), workspace.numel() * workspace.element_size(),

@@ -157,3 +157,18 @@ def test_binding_refuses_tensors_on_the_wrong_side():
     with pytest.raises(ValueError, match="contiguous"):
         qm._hptr(torch.zeros((256, 2)).t())
     assert qm._hptr(host) == host.data_ptr() and qm._dptr(1 << 40) == 1 << 40 and qm._dptr(None) is None
+
+
+def test_binding_refuses_short_x_or_out():
+    """The layer calls check that x and out hold n_tokens rows before the library reads or writes them."""
+    import torch
+    shape = qm.make_shape(256, 8, 2, 256, 256, qm.QS_BF16)
+    ex = qm.make_experts(1 << 40, 64512)
+    x_short = torch.zeros((3, 256), dtype=torch.int16)     # 3 rows of bf16 bits
+    out_ok = torch.zeros((4, 256), dtype=torch.float32)
+    with pytest.raises(ValueError, match="x: 1536 bytes, need 4 rows of 512 bytes"):
+        qm.qs_moe_ffn(shape, x_short, 1 << 40, None, ex, None, out_ok, 4, torch.zeros(16, dtype=torch.uint8))
+    x_ok = torch.zeros((4, 256), dtype=torch.int16)
+    out_short = torch.zeros((4, 255), dtype=torch.float32)
+    with pytest.raises(ValueError, match="out: "):
+        qm.qs_moe_ffn_host(shape, x_ok, 1 << 40, None, ex, None, out_short, 4, torch.zeros(16, dtype=torch.uint8))
