@@ -56,16 +56,18 @@
 namespace qs {
 namespace {
 
-constexpr int kNT = 128;                  // max tokens (B rows, MMA N) per unit
-constexpr int kSlotBytes = 32768;         // one raw slot
-constexpr int kMatStride = 16384;         // second matrix (up) inside a raw slot
-constexpr int kBStageBytes = kNT * 128;   // B operand stage: 128 rows x 64 16-bit values
+constexpr int kNT = 128;                  // max tokens per unit (MMA M: token rows)
+constexpr int kWRows = 256;               // weight rows per unit (MMA N)
 constexpr int kColBox = 112;              // bytes per row of a Q2_K column box (covers 84 + offset <= 12)
-constexpr int kA0 = 256;                  // first TMEM column of the A stages
+constexpr int kHalfSlot = 128 * kColBox;  // 128 rows of a column box
+constexpr int kColSlot = 2 * kHalfSlot;   // raw slot of a column chunk: 256 rows of a column box
+constexpr int kMaxSlot = 32768;           // largest raw slot: 128 whole rows of at most 256 bytes
+constexpr int kABytes = kNT * 128;        // A stage: 128 token rows x 64 16-bit values (128-byte swizzle)
+constexpr int kWBytes = kWRows * 128;     // W stage: 256 weight rows x 64 16-bit values (128-byte swizzle)
 constexpr int kDeqWarps = 16;             // dequant warps of an expert kernel
 constexpr int kWarpMma = kDeqWarps + 4;   // MMA issuer (+ TMEM allocation)
-constexpr int kWarpRaw = kDeqWarps + 5;   // TMA of raw weights
-constexpr int kWarpB = kDeqWarps + 6;     // TMA of B slices
+constexpr int kWarpRaw = kDeqWarps + 5;   // TMA of raw Q2_K weights and of the shared expert's W tiles
+constexpr int kWarpA = kDeqWarps + 6;     // TMA of token rows (the A operand)
 constexpr int kExpertThreads = 32 * (kDeqWarps + 7);
 constexpr int kRouterStages = 3;
 constexpr int kRouterThreads = 192;
@@ -97,6 +99,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
 // x < 2^23 as a float, exactly: x in the mantissa of 2^23, minus 2^23 (no int-to-float conversion).
 __device__ __forceinline__ float small_uint_to_float(uint32_t x) {
     return __uint_as_float(0x4B000000u | x) - 8388608.0f;
+}
+
+// `count` arrivals on an mbarrier at once.
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -144,32 +151,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     if (ok) (void)mbar_try_wait(bar, parity);
     return ok != 0;
 }
-// Bounded wait (lane 0 polls, result broadcast) until *tag == want.
-__device__ __forceinline__ bool warp_wait_tag(const int* tag, int want, volatile int* abort, uint32_t* status,
-                                              uint32_t code = 0) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        const volatile int* t = tag;
-        if (*t != want) {
-            const uint64_t t0 = global_timer_ns();
-            while (*t != want) {
-                __nanosleep(64);
-                if (*abort) {
-                    ok = 0;
-                    break;
-                }
-                if (global_timer_ns() - t0 > kWaitNs) {
-                    *abort = 1;
-                    note_timeout(status, code, (uint32_t)want);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-    }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 // Abort flag as one value for the whole warp (lane 0's reading).
 __device__ __forceinline__ bool warp_aborted(volatile int* abort) {
     return __shfl_sync(0xffffffffu, *abort, 0) != 0;
@@ -477,16 +458,17 @@ __global__ void __launch_bounds__(256) pf_combine_kernel(const uint16_t* __restr
 
 // ================================================================== grouped expert GEMMs
 
-constexpr int kNB = 6;  // B operand stages (shared memory, filled by TMA)
-constexpr int kNRv = 3; // raw weight slots
+constexpr int kMaxNA = 6;  // A stages (token rows, filled by TMA): as many as shared memory holds
+constexpr int kNW = 2;   // W stages (dequantised weight rows, or the shared expert's bf16 rows by TMA)
+constexpr int kNRv = 3;  // raw Q2_K slots
 
 struct ExpertParams {
     CUtensorMap map_q;   // routed Q2_K rows, column mode: u8 [E][rows][rowbytes], box 112 x 128 x 1
     CUtensorMap map_s0;  // shared bf16 matrix 0 (gate, or down): [rows][K], box 64 x 128, 128B swizzle
     CUtensorMap map_s1;  // shared bf16 matrix 1 (up)
-    CUtensorMap map_br[3];  // B of routed units: xs [T*k][H] (gate/up) or h16 [T*k][F] (down), fp16,
+    CUtensorMap map_br[3];  // A of routed units: xs [T*k][H] (gate/up) or h16 [T*k][F] (down), fp16,
                             // boxes of 64 x {128, 64, 32} rows
-    CUtensorMap map_bs[3];  // B of shared units: x [T][H] (gate/up) or hs [T][S] (down), bf16, same boxes
+    CUtensorMap map_bs[3];  // A of shared units: x [T][H] (gate/up) or hs [T][S] (down), bf16, same boxes
     const uint8_t* experts;
     int64_t stride;      // bytes between experts
     int64_t q_off;       // byte offset of the first routed matrix inside an expert
@@ -494,10 +476,12 @@ struct ExpertParams {
     int raw_mode;        // kRawColumn / kRawTile
     int rowbytes;        // routed row bytes = K/256 * 84
     int K, Ks;           // routed / shared contraction length
-    int MT, MTs;         // 128-row output tiles of the routed / shared matrices
+    int MT, MTs;         // output tiles of the routed / shared matrices (128 gate + 128 up rows, or 256 rows)
     int E, k, T, F, S, H;
     int n_sgroups;       // shared-expert token tiles (0 when there is no shared expert)
-    int nt;              // token-tile height (MMA N limit)
+    int nt;              // token-tile height (MMA M)
+    int na;              // A stages
+    int slot;            // raw slot bytes (kColSlot, or 128 whole rows)
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
@@ -510,20 +494,15 @@ struct ExpertParams {
     uint32_t* status;
 };
 
-template <int NM>
 struct ExpertCtl {
-    static constexpr int NSA = (NM == 2) ? 4 : 8;  // A stages in tensor memory
-    uint64_t afull[NSA], aempty[NSA];
-    uint64_t bfull[kNB], bempty[kNB];
-    uint64_t rawfull[kNRv], rawfree_d[kNRv], rawfree_m[kNRv];
+    uint64_t afull[kMaxNA], aempty[kMaxNA];
+    uint64_t wfull[kNW], wempty[kNW];
+    uint64_t rawfull[kNRv], rawfree[kNRv];
     uint64_t accfull[2], accempty[2], drain;
-    int raw_tag[kNRv];  // chunk number a raw slot is being filled with (set before the copy is issued)
     uint32_t tmem;
     int abort;
     int n_groups;
     int pad;
-    int col_row[4][kNT];    // epilogue warp q: per accumulator column, its token (shared) or entry (routed)
-    float col_scale[4][kNT];  // ... and the routing weight / shared gate
 };
 
 // Per-expert tables copied to shared memory at the start: unit-tile prefix, list offset, count.
@@ -537,9 +516,9 @@ struct Unit {
     int shared;  // 1: shared-expert unit
     int e;       // expert (routed)
     int tok0;    // first token (shared) or first entry of the expert's list (routed)
-    int n;       // valid B rows
-    int mt;      // output row tile
-    int brow;    // first B row: token (shared) or sorted entry (routed)
+    int n;       // valid token rows
+    int mt;      // output tile
+    int brow;    // first token row: token (shared) or sorted entry (routed)
 };
 
 // Unit = (group g, output tile m).  Groups are token tiles: the shared expert's first, then each
@@ -571,7 +550,8 @@ __device__ __forceinline__ Unit make_unit(int g, int m, const ExpertParams& p, c
 }
 
 // Iterate this CTA's units in order: body(U) for each; stop early when body returns false.
-// Units (group-major) are dealt to CTAs one by one, for balance.
+// Units (group-major) are dealt to CTAs one by one, for balance; a CTA's shared-expert units
+// come before its routed ones.
 template <class Body>
 __device__ __forceinline__ void for_units(const ExpertParams& p, const ExpertTables& tb, int n_groups, Body body) {
     const int n_su = p.n_sgroups * p.MTs, n_units = n_su + (n_groups - p.n_sgroups) * p.MT;
@@ -582,44 +562,51 @@ __device__ __forceinline__ void for_units(const ExpertParams& p, const ExpertTab
     }
 }
 
-// Per-unit geometry shared by every role.
-struct Geo {
-    int KB;   // 64-wide K slices
-    int nch;  // raw chunks
-    int kpc;  // K slices per chunk
-};
-__device__ __forceinline__ Geo unit_geo(const Unit& U, const ExpertParams& p) {
-    Geo g;
-    if (U.shared) {
-        g.KB = p.Ks / 64;
-        g.nch = g.KB;
-        g.kpc = 1;
-    } else if (p.raw_mode == kRawColumn) {
-        g.KB = p.K / 64;
-        g.nch = p.K / 256;
-        g.kpc = 4;
-    } else {
-        g.KB = p.K / 64;
-        g.nch = 1;
-        g.kpc = g.KB;
-    }
-    return g;
+// 64-wide K slices of a unit, and its raw Q2_K chunks: a column of blocks for all 256 weight
+// rows (column mode), or 128 whole rows (tile mode: two chunks per unit); none for shared units.
+__device__ __forceinline__ int unit_kb(const Unit& U, const ExpertParams& p) { return (U.shared ? p.Ks : p.K) / 64; }
+__device__ __forceinline__ int unit_nch(const Unit& U, const ExpertParams& p) {
+    return U.shared ? 0 : (p.raw_mode == kRawColumn ? p.K / 256 : 2);
 }
 
-// NM = 2: gate+up (two weight matrices share the B operand); NM = 1: down.
-// Warps 0..15 dequantise (routed units), 16..19 epilogue, 20 MMA (+TMEM), 21 TMA of raw weights,
-// 22 TMA of B slices.
+// One thread's half row of a W stage: the 16 words (32 fp16 weights, K positions 32 jj .. 32 jj + 31
+// of the slice) of weight row r, stored at their 128-byte-swizzled places.
+__device__ __forceinline__ void store_w_half(uint8_t* wst, int r, int jj, const uint32_t (&v)[16]) {
+    const uint32_t row = smem_u32(wst) + (uint32_t)r * 128u;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const uint32_t a = row + ((uint32_t)((4 * jj + i) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v[4 * i]), "r"(v[4 * i + 1]),
+                     "r"(v[4 * i + 2]), "r"(v[4 * i + 3])
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
+// NM = 2: gate+up (the unit's W rows are 128 gate rows, then the same 128 up rows);
+// NM = 1: down (256 rows of one matrix).  D[token][weight row] accumulates in tensor memory
+// (M = 128 token rows, N = 256 weight rows per MMA; two accumulator buffers).
+// Warps 0..15 dequantise (routed units), 16..19 epilogue, 20 MMA (+TMEM), 21 TMA of raw weights
+// and of the shared expert's W tiles, 22 TMA of token rows.
 template <int NM>
 __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __grid_constant__ ExpertParams p) {
-    using Ctl = ExpertCtl<NM>;
-    constexpr int NSA = Ctl::NSA;
-    constexpr int NAB = (NM == 2) ? 1 : 2;           // accumulator buffers
-    constexpr int kDeqPerSlice = (NM == 2) ? 8 : 4;  // dequant warps writing one A stage
     extern __shared__ uint8_t ex_smem_raw[];
     uint8_t* sm = align1024(ex_smem_raw);
-    uint8_t* raw = sm;
-    uint8_t* bst = sm + kNRv * kSlotBytes;
-    Ctl* ctl = reinterpret_cast<Ctl*>(bst + kNB * kBStageBytes);
+    const int NA = p.na, SLOT = p.slot;
+    uint8_t* ast = sm;                       // NA x kABytes
+    uint8_t* wst = ast + NA * kABytes;       // kNW x kWBytes
+    uint8_t* raw = wst + kNW * kWBytes;      // kNRv x SLOT
+    ExpertCtl* ctl = reinterpret_cast<ExpertCtl*>(raw + kNRv * SLOT);
     ExpertTables tb;
     tb.prefix = reinterpret_cast<int*>(ctl + 1);
     tb.offs = tb.prefix + p.E + 1;
@@ -628,25 +615,23 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSA; s++) {
-            mbar_init(&ctl->afull[s], kDeqPerSlice);
+        for (int s = 0; s < NA; s++) {
+            mbar_init(&ctl->afull[s], 1);
             mbar_init(&ctl->aempty[s], 1);
         }
-        for (int s = 0; s < kNB; s++) {
-            mbar_init(&ctl->bfull[s], 1);
-            mbar_init(&ctl->bempty[s], 1);
+        for (int s = 0; s < kNW; s++) {
+            mbar_init(&ctl->wfull[s], kDeqWarps);
+            mbar_init(&ctl->wempty[s], 1);
         }
         for (int r = 0; r < kNRv; r++) {
             mbar_init(&ctl->rawfull[r], 1);
-            mbar_init(&ctl->rawfree_d[r], kDeqWarps);
-            mbar_init(&ctl->rawfree_m[r], 1);
+            mbar_init(&ctl->rawfree[r], kDeqWarps);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&ctl->accfull[b], 1);
             mbar_init(&ctl->accempty[b], 4);
         }
         mbar_init(&ctl->drain, 1);
-        for (int r = 0; r < kNRv; r++) ctl->raw_tag[r] = -1;
         ctl->abort = 0;
         fence_barrier_init();
     }
@@ -684,163 +669,178 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
     const int n_groups = ctl->n_groups;
 
     if (warp < kDeqWarps) {
-        // ---------------------------------------------------------- dequant warps: raw slot -> TMEM A stage
-        // Warp w writes TMEM lane quarter q = w % 4 (rows 32q..32q+31) of matrix m (gate/up: bit 2
-        // of w) for the K slices kb with kb % n_slice_groups == its group.
-        const int q = warp & 3, r = 32 * q + lane;
-        const int m = (NM == 2) ? ((warp >> 2) & 1) : 0;
-        constexpr int kSliceGroups = (NM == 2) ? kDeqWarps / 8 : kDeqWarps / 4;
-        const int grp = (NM == 2) ? (warp >> 3) : (warp >> 2);
-        int G = 0, C = 0;
-        int pend = -1;  // A stage whose tensor-memory store was issued but not yet signalled
-        auto flush = [&]() {
-            if (pend >= 0) {
-                tc::wait_st();
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->afull[pend]);
-                pend = -1;
-            }
-        };
+        // ---------------------------------------------------------- dequant warps: raw slot -> W stage
+        // Thread: weight row r of the unit (gate/up: rows 0..127 gate, 128..255 up), K half jj of
+        // every slice.  A stage is full once all sixteen warps have stored their rows.
+        const int r = 32 * (warp & 7) + lane, jj = warp >> 3;
+        int GW = 0, C = 0;
         for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
             if (warp_aborted(abort)) return false;
-            const Geo g = unit_geo(U, p);
-            if (U.shared) {  // the MMA reads shared-expert tiles straight from the raw slots
-                C += g.nch;
+            const int KB = unit_kb(U, p);
+            if (U.shared) {  // the raw-weight thread loads these W tiles
+                GW += KB;
                 return true;
             }
-            const int nblk = (p.raw_mode == kRawColumn) ? 1 : p.K / 256;  // Q2_K blocks per row per chunk
-            bool ok = true;
-            for (int ch = 0; ch < g.nch && ok; ch++, C++) {
-                const int slot = C % kNRv;
-                // Shared-expert chunks in between are consumed by the MMA, not by these warps, so
-                // they can be two fills ahead of the slot: wait for the slot to be tagged with this
-                // chunk before the phase-parity wait, which cannot tell phases two apart.
-                ok = warp_wait_tag(&ctl->raw_tag[slot], C, abort, p.status, 2) &&
-                     warp_wait(&ctl->rawfull[slot], (C / kNRv) & 1, abort, p.status, 1, C);
-                if (!ok) break;
-                const uint8_t* sl = raw + slot * kSlotBytes + m * kMatStride;
+            // one 64-wide slice: weights of row r from the block words w[] -> W stage (GW + kb)
+            auto slice = [&](int kb, int c, uint32_t scw, const uint32_t (&qw)[8], float d, float dm) -> bool {
+                const int g = GW + kb, s = g % kNW;
+                uint32_t v[16];
+                dequant_half(scw, qw, c, jj, d, dm, v);
+                if (g >= kNW && !warp_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 3, g)) return false;
+                store_w_half(wst + s * kWBytes, r, jj, v);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->wfull[s]);
+                return true;
+            };
+            if (p.raw_mode == kRawColumn) {
+                const int nch = p.K / 256;
 #pragma unroll 1
-                for (int blk = 0; blk < nblk && ok; blk++) {
-                    uint32_t w[21];
-                    if (p.raw_mode == kRawColumn) {
-                        uint32_t win[24];
-                        const uint8_t* row = sl + r * kColBox;
+                for (int ch = 0; ch < nch; ch++, C++) {
+                    const int slot = C % kNRv;
+                    if (!warp_wait(&ctl->rawfull[slot], (C / kNRv) & 1, abort, p.status, 1, C)) return false;
+                    // the block starts (84 ch) mod 16 bytes into the 112-byte row of the column box
+                    const uint32_t row = smem_u32(raw + slot * SLOT) + (uint32_t)r * kColBox;
+                    uint32_t win[24], w[21];
 #pragma unroll
-                        for (int c = 0; c < 6; c++) {
-                            const uint4 x4 = *reinterpret_cast<const uint4*>(row + 16 * c);
-                            win[4 * c] = x4.x;
-                            win[4 * c + 1] = x4.y;
-                            win[4 * c + 2] = x4.z;
-                            win[4 * c + 3] = x4.w;
-                        }
-                        switch (((84 * ch) & 15) >> 2) {
+                    for (int i = 0; i < 6; i++) {
+                        const uint4 x4 = lds128(row + 16 * i);
+                        win[4 * i] = x4.x;
+                        win[4 * i + 1] = x4.y;
+                        win[4 * i + 2] = x4.z;
+                        win[4 * i + 3] = x4.w;
+                    }
+                    switch (ch & 3) {
 #define QS_SEL(O) \
     case O:       \
         _Pragma("unroll") for (int i = 0; i < 21; i++) w[i] = win[i + O]; \
         break;
-                            QS_SEL(0) QS_SEL(1) QS_SEL(2) QS_SEL(3)
+                        QS_SEL(0) QS_SEL(1) QS_SEL(2) QS_SEL(3)
 #undef QS_SEL
-                        }
-                    } else {
-                        const uint32_t* row = reinterpret_cast<const uint32_t*>(sl + (size_t)r * p.rowbytes + 84 * blk);
-#pragma unroll
-                        for (int i = 0; i < 21; i++) w[i] = row[i];
                     }
                     const float d = __half2float(__ushort_as_half((unsigned short)(w[20] & 0xffffu)));
                     const float dm = __half2float(__ushort_as_half((unsigned short)(w[20] >> 16)));
-                    const int kb0 = (p.raw_mode == kRawColumn ? 4 * ch : 4 * blk);
-#pragma unroll 1
-                    for (int c = 0; c < 4 && ok; c++) {
-                        const int kb = kb0 + c;
-                        if (kb % kSliceGroups != grp) continue;
-                        const uint32_t scw = (c == 0) ? w[0] : (c == 1) ? w[1] : (c == 2) ? w[2] : w[3];
-                        uint32_t qw[8];
+                    uint32_t q0[8], q1[8];
 #pragma unroll
-                        for (int i = 0; i < 8; i++) qw[i] = (c >= 2) ? w[12 + i] : w[4 + i];
-                        uint32_t v[16];
-                        dequant_half(scw, qw, c, 0, d, dm, v);
-                        // signal the previous slice (its stores have overlapped this slice's
-                        // dequantisation), wait for this slice's A stage, store this row's 32 columns
-                        const int Gk = G + kb, s = Gk % NSA;
-                        flush();
-                        if (Gk >= NSA && !warp_wait(&ctl->aempty[s], ((Gk / NSA) - 1) & 1, abort, p.status, 3, Gk)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::fence_after();
-                        const uint32_t ta = tc::taddr(tbase, 32 * q, kA0 + s * 32 * NM + m * 32);
-                        tc::st16(ta, v);
-                        dequant_half(scw, qw, c, 1, d, dm, v);
-                        tc::st16(ta + 16, v);
-                        pend = s;
+                    for (int i = 0; i < 8; i++) {
+                        q0[i] = w[4 + i];
+                        q1[i] = w[12 + i];
                     }
+                    if (!slice(4 * ch + 0, 0, w[0], q0, d, dm) || !slice(4 * ch + 1, 1, w[1], q0, d, dm) ||
+                        !slice(4 * ch + 2, 2, w[2], q1, d, dm) || !slice(4 * ch + 3, 3, w[3], q1, d, dm))
+                        return false;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->rawfree[slot]);
+                }
+            } else {
+                // tile mode: chunk C holds rows 0..127, chunk C + 1 rows 128..255, each whole
+                const int mine = C + (r >> 7), slot = mine % kNRv;
+                if (!warp_wait(&ctl->rawfull[C % kNRv], (C / kNRv) & 1, abort, p.status, 1, C) ||
+                    !warp_wait(&ctl->rawfull[(C + 1) % kNRv], ((C + 1) / kNRv) & 1, abort, p.status, 1, C + 1))
+                    return false;
+                const uint32_t row = smem_u32(raw + slot * SLOT) + (uint32_t)(r & 127) * p.rowbytes;
+#pragma unroll 1
+                for (int kb = 0; kb < KB; kb++) {
+                    const uint32_t blk = row + 84u * (uint32_t)(kb >> 2);
+                    const int c = kb & 3;
+                    uint32_t qw[8];
+#pragma unroll
+                    for (int i = 0; i < 8; i++) qw[i] = lds32(blk + 4u * (4 + 8 * (c >> 1) + i));
+                    const uint32_t dd = lds32(blk + 80u);
+                    const float d = __half2float(__ushort_as_half((unsigned short)(dd & 0xffffu)));
+                    const float dm = __half2float(__ushort_as_half((unsigned short)(dd >> 16)));
+                    if (!slice(kb, c, lds32(blk + 4u * c), qw, d, dm)) return false;
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->rawfree_d[slot]);
+                if (lane == 0) {
+                    mbar_arrive(&ctl->rawfree[C % kNRv]);
+                    mbar_arrive(&ctl->rawfree[(C + 1) % kNRv]);
+                }
+                C += 2;
             }
-            flush();  // before the next unit: the MMA must be able to finish this one
-            G += g.KB;
-            return ok;
+            GW += KB;
+            return true;
         });
-        flush();
     } else if (warp < kWarpMma) {
         // ---------------------------------------------------------- epilogue warps
-        const int q = warp & 3, row = 32 * q + lane;
-        int* crow = ctl->col_row[q];
-        float* cscale = ctl->col_scale[q];
+        // Thread: token row m = 32 q + lane of the unit (its accumulator lane).
+        const int q = warp & 3, m = 32 * q + lane;
         int V = 0;
         for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
             if (warp_aborted(abort)) return false;
-            const int b = V % NAB;
-            if (NM == 1) {  // column metadata of this unit, read back as broadcasts below
-                for (int n = lane; n < U.n; n += 32) {
-                    if (U.shared) {
-                        crow[n] = U.tok0 + n;
-                        cscale[n] = p.gate_s[U.tok0 + n];
-                    } else {
-                        const int ent = p.perm[U.brow + n];
-                        crow[n] = ent;
-                        cscale[n] = p.pw[ent];
-                    }
+            const int b = V & 1;
+            const bool valid = m < U.n;
+            // this row's destination and scale (read before the wait)
+            int dst_row = 0;
+            float scale = 1.0f;
+            if (valid) {
+                if (U.shared) {
+                    dst_row = U.tok0 + m;
+                    if (NM == 1) scale = p.gate_s[dst_row];
+                } else if (NM == 2) {
+                    dst_row = U.brow + m;
+                } else {
+                    dst_row = p.perm[U.brow + m];
+                    scale = p.pw[dst_row];
                 }
-                __syncwarp();
             }
-            if (!warp_wait(&ctl->accfull[b], (V / NAB) & 1, abort, p.status, 4, V)) return false;
+            if (!warp_wait(&ctl->accfull[b], (V >> 1) & 1, abort, p.status, 4, V)) return false;
             tc::fence_after();
-            const int o = U.mt * 128 + row;  // output feature (gate/up: f; down: h)
+            const uint32_t tacc = tc::taddr(tbase, 32 * q, b * 256);
             if (NM == 2) {
-                uint16_t* dst = U.shared ? p.out_hs + (size_t)U.tok0 * p.S + o : p.out_h + (size_t)U.brow * p.F + o;
-                const size_t ld = U.shared ? (size_t)p.S : (size_t)p.F;
+                uint16_t* dst = U.shared ? p.out_hs + (size_t)dst_row * p.S + U.mt * 128
+                                         : p.out_h + (size_t)dst_row * p.F + U.mt * 128;
 #pragma unroll 1
-                for (int c0 = 0; c0 < U.n; c0 += 16) {  // warp-uniform
+                for (int j0 = 0; j0 < 128; j0 += 16) {
                     uint32_t gv[16], uv[16];
-                    tc::ld16(tc::taddr(tbase, 32 * q, c0), gv);
-                    tc::ld16(tc::taddr(tbase, 32 * q, 128 + c0), uv);
+                    tc::ld16(tacc + j0, gv);
+                    tc::ld16(tacc + 128 + j0, uv);
                     tc::wait_ld();
+                    if (valid) {
+                        uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        if (c0 + i < U.n) {
-                            const float gq = __uint_as_float(gv[i]);
-                            const float hv = __fdividef(gq, 1.0f + __expf(-gq)) * __uint_as_float(uv[i]);
-                            dst[(size_t)(c0 + i) * ld] = U.shared ? __bfloat16_as_ushort(__float2bfloat16_rn(hv))
-                                                                  : __half_as_ushort(__float2half_rn(hv));
+                        for (int i = 0; i < 8; i++) {
+                            float hv[2];
+#pragma unroll
+                            for (int h = 0; h < 2; h++) {
+                                const float gq = __uint_as_float(gv[2 * i + h]);
+                                hv[h] = __fdividef(gq, 1.0f + __expf(-gq)) * __uint_as_float(uv[2 * i + h]);
+                            }
+                            if (U.shared) {
+                                const __nv_bfloat162 t2 = __floats2bfloat162_rn(hv[0], hv[1]);
+                                pk[i] = *reinterpret_cast<const uint32_t*>(&t2);
+                            } else {
+                                pk[i] = pack_h2(hv[0], hv[1]);
+                            }
                         }
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + j0);
+#pragma unroll
+                        for (int i = 0; i < 2; i++) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                     }
                 }
             } else {
 #pragma unroll 1
-                for (int c0 = 0; c0 < U.n; c0 += 32) {  // warp-uniform
+                for (int j0 = 0; j0 < 256; j0 += 32) {
                     uint32_t av[32];
-                    tc::ld32(tc::taddr(tbase, 32 * q, b * 128 + c0), av);
+                    tc::ld32(tacc + j0, av);
                     tc::wait_ld();
+                    if (valid) {
+                        if (U.shared) {
+                            float4* d4 = reinterpret_cast<float4*>(p.y + (size_t)dst_row * p.H + U.mt * 256 + j0);
 #pragma unroll
-                    for (int i = 0; i < 32; i++) {
-                        if (c0 + i < U.n) {
-                            const int rr = crow[c0 + i];  // token (shared) or entry (routed)
-                            const float v = cscale[c0 + i] * __uint_as_float(av[i]);
-                            if (U.shared) p.y[(size_t)rr * p.H + o] = v;
-                            else p.yp[(size_t)rr * p.H + o] = __half_as_ushort(__float2half_rn(v));
+                            for (int i = 0; i < 8; i++)
+                                d4[i] = make_float4(scale * __uint_as_float(av[4 * i]), scale * __uint_as_float(av[4 * i + 1]),
+                                                    scale * __uint_as_float(av[4 * i + 2]),
+                                                    scale * __uint_as_float(av[4 * i + 3]));
+                        } else {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int i = 0; i < 16; i++)
+                                pk[i] = pack_h2(scale * __uint_as_float(av[2 * i]), scale * __uint_as_float(av[2 * i + 1]));
+                            uint4* d4 = reinterpret_cast<uint4*>(p.yp + (size_t)dst_row * p.H + U.mt * 256 + j0);
+#pragma unroll
+                            for (int i = 0; i < 4; i++)
+                                d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                         }
                     }
                 }
@@ -853,63 +853,38 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         });
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issuer
-        // The whole warp runs the loop (its values are warp-uniform, so the MMA operands need no
-        // per-instruction move into the uniform datapath); lane 0 issues the MMAs and commits.
+        // The whole warp runs the loop (its values are warp-uniform); lane 0 issues the MMAs and
+        // the commits.  Per slice: four M = 128, N = 256, K = 16 MMAs into accumulator buffer V % 2.
         const uint32_t tmu = __shfl_sync(0xffffffffu, tbase, 0);
         const bool leader = lane == 0;
-        int GA = 0, GB = 0, C = 0, V = 0;
+        int GA = 0, GW = 0, V = 0;
         for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
             if (warp_aborted(abort)) return false;
-            const Geo g = unit_geo(U, p);
-            const int b = V % NAB;
-            if (V >= NAB && !warp_wait(&ctl->accempty[b], ((V / NAB) - 1) & 1, abort, p.status, 5, V)) return false;
+            const int KB = unit_kb(U, p);
+            const int b = V & 1;
+            if (V >= 2 && !warp_wait(&ctl->accempty[b], ((V >> 1) - 1) & 1, abort, p.status, 5, V)) return false;
             tc::fence_after();
-            const int nmma = max(16, (U.n + 15) & ~15);
-            const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, 128, nmma);
-            for (int kb = 0; kb < g.KB; kb++) {
-                const int sb = (GB + kb) % kNB;
-                if (!warp_wait(&ctl->bfull[sb], ((GB + kb) / kNB) & 1, abort, p.status, 6, GB + kb)) return false;
-                const uint64_t bd = tc::sdesc_sw128(smem_u32(bst + sb * kBStageBytes));
-                if (U.shared) {
-                    const int c = C + kb, slot = c % kNRv;
-                    if (!warp_wait(&ctl->rawfull[slot], (c / kNRv) & 1, abort, p.status, 7, c)) return false;
-                    tc::fence_after();
-                    const uint32_t sa = smem_u32(raw + slot * kSlotBytes);
-                    if (leader) {
+            const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, kNT, kWRows);
+            const uint32_t d = tmu + b * 256;
+            for (int kb = 0; kb < KB; kb++) {
+                const int ga = GA + kb, sa = ga % NA, gw = GW + kb, sw = gw % kNW;
+                if (!warp_wait(&ctl->afull[sa], (ga / NA) & 1, abort, p.status, 6, ga)) return false;
+                if (!warp_wait(&ctl->wfull[sw], (gw / kNW) & 1, abort, p.status, 8, gw)) return false;
+                tc::fence_after();
+                if (leader) {
+                    const uint64_t ad = tc::sdesc_sw128(smem_u32(ast + sa * kABytes));
+                    const uint64_t bd = tc::sdesc_sw128(smem_u32(wst + sw * kWBytes));
 #pragma unroll
-                        for (int mq = 0; mq < NM; mq++) {
-                            const uint32_t d = tmu + (NM == 2 ? mq * 128 : b * 128);
-                            const uint64_t ad = tc::sdesc_sw128(sa + mq * kMatStride);
-#pragma unroll
-                            for (int k16 = 0; k16 < 4; k16++)
-                                tc::mma_ss_f16(d, ad + 2 * k16, bd + 2 * k16, id, (kb | k16) != 0);
-                        }
-                        tc::commit(&ctl->rawfree_m[slot]);
-                    }
-                } else {
-                    const int Gk = GA + kb, s = Gk % NSA;
-                    if (!warp_wait(&ctl->afull[s], (Gk / NSA) & 1, abort, p.status, 8, Gk)) return false;
-                    tc::fence_after();
-                    if (leader) {
-#pragma unroll
-                        for (int mq = 0; mq < NM; mq++) {
-                            const uint32_t d = tmu + (NM == 2 ? mq * 128 : b * 128);
-                            const uint32_t a = tmu + kA0 + s * 32 * NM + mq * 32;
-#pragma unroll
-                            for (int k16 = 0; k16 < 4; k16++)
-                                tc::mma_ts_f16(d, a + 8 * k16, bd + 2 * k16, id, (kb | k16) != 0);
-                        }
-                        tc::commit(&ctl->aempty[s]);
-                    }
+                    for (int k16 = 0; k16 < 4; k16++) tc::mma_ss_f16(d, ad + 2 * k16, bd + 2 * k16, id, (kb | k16) != 0);
+                    tc::commit(&ctl->aempty[sa]);
+                    tc::commit(&ctl->wempty[sw]);
                 }
-                if (leader) tc::commit(&ctl->bempty[sb]);
                 __syncwarp();
             }
             if (leader) tc::commit(&ctl->accfull[b]);
             __syncwarp();
-            GB += g.KB;
-            C += g.nch;
-            if (!U.shared) GA += g.KB;
+            GA += KB;
+            GW += KB;
             V++;
             return true;
         });
@@ -919,67 +894,76 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         }
         __syncwarp();
     } else {
-        // ---------------------------------------------------------- TMA: raw weights (warp 13), B slices (warp 14)
-        const bool do_raw = (warp == kWarpRaw), do_b = (warp == kWarpB);
+        // ---------------------------------------------------------- TMA: raw weights + shared W tiles (warp 21),
+        // token rows (warp 22)
+        const bool do_raw = (warp == kWarpRaw), do_a = (warp == kWarpA);
         if (lane == 0) {
-            int C = 0, GB = 0;
-            int used_d[kNRv] = {}, used_m[kNRv] = {}, last_use[kNRv];  // last consumer: 0 none, 1 dequant, 2 MMA
-            for (int i = 0; i < kNRv; i++) last_use[i] = 0;
+            int C = 0, GW = 0, GA = 0;
+            int wt_last[kNW];  // per W stage, the last fill this thread issued (-1: none)
+            for (int i = 0; i < kNW; i++) wt_last[i] = -1;
             for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
                 if (*abort) return false;
-                const Geo g = unit_geo(U, p);
-                const int row0 = U.mt * 128;
-                for (int kb = 0; kb < g.KB; kb++) {
-                    if (do_raw && kb % g.kpc == 0) {  // next raw chunk
-                        const int ch = kb / g.kpc, slot = C % kNRv;
-                        bool ok = true;
-                        if (last_use[slot] == 1) {
-                            ok = thread_wait(&ctl->rawfree_d[slot], used_d[slot] & 1, abort, p.status, 9, C);
-                            used_d[slot]++;
-                        } else if (last_use[slot] == 2) {
-                            ok = thread_wait(&ctl->rawfree_m[slot], used_m[slot] & 1, abort, p.status, 10, C);
-                            used_m[slot]++;
+                const int KB = unit_kb(U, p);
+                if (do_raw && U.shared) {
+                    // the shared expert's bf16 rows are the W operand as they land: two 128-row boxes
+                    for (int kb = 0; kb < KB; kb++) {
+                        const int g = GW + kb, s = g % kNW;
+                        if (g >= kNW && !thread_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 10, g))
+                            return false;
+                        uint8_t* w = wst + s * kWBytes;
+                        uint64_t* bar = &ctl->wfull[s];
+                        wt_last[s] = g;
+                        mbar_arrive_expect_tx(bar, kWBytes);
+                        mbar_arrive_count(bar, kDeqWarps - 1);
+                        if (NM == 2) {
+                            tma_load_2d(w, &p.map_s0, kb * 64, U.mt * 128, bar);
+                            tma_load_2d(w + kWBytes / 2, &p.map_s1, kb * 64, U.mt * 128, bar);
+                        } else {
+                            tma_load_2d(w, &p.map_s0, kb * 64, U.mt * 256, bar);
+                            tma_load_2d(w + kWBytes / 2, &p.map_s0, kb * 64, U.mt * 256 + 128, bar);
                         }
-                        if (!ok) return false;
-                        last_use[slot] = U.shared ? 2 : 1;
-                        *reinterpret_cast<volatile int*>(&ctl->raw_tag[slot]) = C;
-                        uint8_t* sl = raw + slot * kSlotBytes;
+                    }
+                } else if (do_raw) {
+                    const int nch = unit_nch(U, p);
+                    for (int ch = 0; ch < nch; ch++, C++) {
+                        const int slot = C % kNRv;
+                        if (C >= kNRv && !thread_wait(&ctl->rawfree[slot], ((C / kNRv) - 1) & 1, abort, p.status, 9, C))
+                            return false;
+                        uint8_t* sl = raw + slot * SLOT;
                         uint64_t* bar = &ctl->rawfull[slot];
-                        if (U.shared) {
-                            mbar_arrive_expect_tx(bar, NM * 16384);
-                            tma_load_2d(sl, &p.map_s0, ch * 64, row0, bar);
-                            if (NM == 2) tma_load_2d(sl + kMatStride, &p.map_s1, ch * 64, row0, bar);
-                        } else if (p.raw_mode == kRawColumn) {
-                            mbar_arrive_expect_tx(bar, NM * kColBox * 128);
+                        if (p.raw_mode == kRawColumn) {
                             const int x0 = (84 * ch) & ~15;
-                            tma_load_3d(sl, &p.map_q, x0, row0, U.e, bar);
-                            if (NM == 2) tma_load_3d(sl + kMatStride, &p.map_q, x0, p.q_rows_m1 + row0, U.e, bar);
+                            const int r0 = (NM == 2) ? U.mt * 128 : U.mt * 256;
+                            const int r1 = (NM == 2) ? p.q_rows_m1 + U.mt * 128 : U.mt * 256 + 128;
+                            mbar_arrive_expect_tx(bar, kColSlot);
+                            tma_load_3d(sl, &p.map_q, x0, r0, U.e, bar);
+                            tma_load_3d(sl + kHalfSlot, &p.map_q, x0, r1, U.e, bar);
                         } else {
                             const uint32_t bytes = 128u * (uint32_t)p.rowbytes;
-                            mbar_arrive_expect_tx(bar, NM * bytes);
-                            const uint8_t* src =
-                                p.experts + (size_t)U.e * p.stride + p.q_off + (size_t)row0 * p.rowbytes;
-                            bulk_g2s(sl, src, bytes, bar);
-                            if (NM == 2) bulk_g2s(sl + kMatStride, src + (size_t)p.q_rows_m1 * p.rowbytes, bytes, bar);
+                            const int row = (NM == 2) ? (ch == 0 ? 0 : p.q_rows_m1) + U.mt * 128 : U.mt * 256 + 128 * ch;
+                            mbar_arrive_expect_tx(bar, bytes);
+                            bulk_g2s(sl, p.experts + (size_t)U.e * p.stride + p.q_off + (size_t)row * p.rowbytes, bytes,
+                                     bar);
                         }
-                        C++;
                     }
-                    // B slice: the unit's rows only (one 128-row box, or 64 and/or 32-row boxes),
-                    // once the stage's previous slice is released.
-                    if (!do_b) continue;
-                    const int sb = GB % kNB;
-                    if (GB >= kNB && !thread_wait(&ctl->bempty[sb], ((GB / kNB) - 1) & 1, abort, p.status, 11, GB))
-                        return false;
+                }
+                GW += KB;
+                if (do_a) {
+                    // token rows: the unit's rows only (one 128-row box, or 64 and/or 32-row boxes)
                     const CUtensorMap* mp = U.shared ? p.map_bs : p.map_br;
-                    uint8_t* bs = bst + sb * kBStageBytes;
                     const int r128 = U.n > 96 ? 128 : 0;
                     const int r64 = (r128 == 0 && U.n > 32) ? 64 : 0;
                     const int r32 = (r128 == 0 && U.n - r64 > 0) ? 32 : 0;
-                    mbar_arrive_expect_tx(&ctl->bfull[sb], (uint32_t)(r128 + r64 + r32) * 128u);
-                    if (r128) tma_load_2d(bs, &mp[0], kb * 64, U.brow, &ctl->bfull[sb]);
-                    if (r64) tma_load_2d(bs, &mp[1], kb * 64, U.brow, &ctl->bfull[sb]);
-                    if (r32) tma_load_2d(bs + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->bfull[sb]);
-                    GB++;
+                    for (int kb = 0; kb < KB; kb++, GA++) {
+                        const int s = GA % NA;
+                        if (GA >= NA && !thread_wait(&ctl->aempty[s], ((GA / NA) - 1) & 1, abort, p.status, 11, GA))
+                            return false;
+                        uint8_t* as = ast + s * kABytes;
+                        mbar_arrive_expect_tx(&ctl->afull[s], (uint32_t)(r128 + r64 + r32) * 128u);
+                        if (r128) tma_load_2d(as, &mp[0], kb * 64, U.brow, &ctl->afull[s]);
+                        if (r64) tma_load_2d(as, &mp[1], kb * 64, U.brow, &ctl->afull[s]);
+                        if (r32) tma_load_2d(as + r64 * 128, &mp[2], kb * 64, U.brow + r64, &ctl->afull[s]);
+                    }
                 }
                 return true;
             });
@@ -988,9 +972,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     const int c = C - i;
                     (void)mbar_wait(&ctl->rawfull[c % kNRv], (c / kNRv) & 1, 1000000ull);
                 }
-                for (int i = 1; do_b && i <= kNB && i <= GB; i++) {
-                    const int c = GB - i;
-                    (void)mbar_wait(&ctl->bfull[c % kNB], (c / kNB) & 1, 1000000ull);
+                for (int s = 0; do_raw && s < kNW; s++)
+                    if (wt_last[s] >= 0) (void)mbar_wait(&ctl->wfull[s], (wt_last[s] / kNW) & 1, 1000000ull);
+                for (int i = 1; do_a && i <= NA && i <= GA; i++) {
+                    const int c = GA - i;
+                    (void)mbar_wait(&ctl->afull[c % NA], (c / NA) & 1, 1000000ull);
                 }
             }
         }
@@ -1046,11 +1032,12 @@ bool encode_b(CUtensorMap* m3, CUtensorMapDataType dt, const void* base, int K, 
            encode_rows16(&m3[2], dt, base, K, rows, 32);
 }
 
-// Raw-weight staging mode for a Q2_K matrix with contraction length K, or -1.
-int raw_mode_for(int K, int nm) {
+// Raw-weight staging mode for a Q2_K matrix with contraction length K, or -1: column boxes of
+// 112 bytes when rows are a multiple of 16 bytes, else 128 whole rows per raw slot.
+int raw_mode_for(int K) {
     const int rowbytes = K / 256 * 84;
     if (rowbytes % 16 == 0) return kRawColumn;
-    if (128 * rowbytes <= (nm == 2 ? kMatStride : kSlotBytes)) return kRawTile;
+    if (128 * rowbytes <= kMaxSlot) return kRawTile;
     return -1;
 }
 
@@ -1078,16 +1065,28 @@ cudaError_t pf_facts(PfFacts** out) {
     return cudaSuccess;
 }
 
-template <int NM>
-size_t expert_smem(int E) {
-    return 1024 + kNRv * kSlotBytes + kNB * kBStageBytes + sizeof(ExpertCtl<NM>) + 4 * (3 * E + 1);
+// Dynamic shared memory of an expert kernel with na A stages and raw slots of `slot` bytes.
+size_t expert_smem(int E, int na, int slot) {
+    return 1024 + (size_t)na * kABytes + (size_t)kNW * kWBytes + (size_t)kNRv * slot + sizeof(ExpertCtl) +
+           4 * (3 * (size_t)E + 1);
+}
+// Raw slot bytes for contraction length K (a column chunk, or 128 whole rows).
+int slot_for(int K) {
+    const int rowbytes = K / 256 * 84;
+    return raw_mode_for(K) == kRawColumn ? kColSlot : 128 * rowbytes;
+}
+// A stages that fit beside the rest (0: the kernel does not fit at all).
+int stages_for(int E, int slot, size_t smem_optin) {
+    int na = kMaxNA;
+    while (na >= 2 && expert_smem(E, na, slot) > smem_optin) na--;
+    return na >= 2 ? na : 0;
 }
 size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCtl); }
 
 // Launch one expert kernel, one CTA per SM.
 template <int NM>
 cudaError_t launch_expert(ExpertParams& p, int n_sm, int E, cudaStream_t st) {
-    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem<NM>(E), st>>>(p);
+    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem(E, p.na, p.slot), st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1102,8 +1101,9 @@ int router_splits(int E, int T, int H, int n_sm) {
 
 bool prefill_shape_ok(const qs_moe_shape& s) {
     if (s.x_dtype != QS_BF16) return false;
-    if (raw_mode_for(s.hidden, 2) < 0 || raw_mode_for(s.expert_ffn, 1) < 0) return false;
-    if (s.shared_ffn % 128) return false;
+    if (raw_mode_for(s.hidden) < 0 || raw_mode_for(s.expert_ffn) < 0) return false;
+    // units: 128 gate + 128 up rows (gate/up), 256 rows (down)
+    if (s.expert_ffn % 128 || s.hidden % 256 || s.shared_ffn % 128) return false;
     return true;
 }
 
@@ -1120,19 +1120,19 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
     const int H = s.hidden, E = s.n_experts, k = s.top_k, F = s.expert_ffn;
     const int S = (sg != nullptr) ? s.shared_ffn : 0;
     const int n = T * k;
-    if ((size_t)f->smem_optin < expert_smem<2>(1024) || (size_t)f->smem_optin < expert_smem<1>(1024) ||
-        (size_t)f->smem_optin < router_smem())
-        return cudaErrorNotSupported;
+    const int na2 = stages_for(E, slot_for(H), (size_t)f->smem_optin);
+    const int na1 = stages_for(E, slot_for(F), (size_t)f->smem_optin);
+    if (na2 == 0 || na1 == 0 || (size_t)f->smem_optin < router_smem()) return cudaErrorNotSupported;
     if (!get_encode()) return cudaErrorNotSupported;
     if (!f->attr_set) {
         if ((e = cudaFuncSetAttribute(pf_router_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)router_smem())) != cudaSuccess)
             return e;
         if ((e = cudaFuncSetAttribute(pf_expert_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)expert_smem<2>(1024))) != cudaSuccess)
+                                      f->smem_optin)) != cudaSuccess)
             return e;
         if ((e = cudaFuncSetAttribute(pf_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)expert_smem<1>(1024))) != cudaSuccess)
+                                      f->smem_optin)) != cudaSuccess)
             return e;
         f->attr_set = true;
     }
@@ -1167,7 +1167,9 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         memset(&p, 0, sizeof(p));
         const int K = (nm == 2) ? H : F;
         const int rowbytes = K / 256 * 84;
-        p.raw_mode = raw_mode_for(K, nm);
+        p.raw_mode = raw_mode_for(K);
+        p.slot = slot_for(K);
+        p.na = (nm == 2) ? na2 : na1;
         p.rowbytes = rowbytes;
         p.experts = experts;
         p.stride = stride;
@@ -1185,7 +1187,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         if (!encode_b(p.map_br, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, nm == 2 ? xs : h16, K, n))
             return cudaErrorInvalidValue;
         p.K = K;
-        p.MT = ((nm == 2) ? F : H) / 128;
+        p.MT = (nm == 2) ? F / 128 : H / 256;
         p.nt = kNT;
         p.E = E;
         p.k = k;
@@ -1195,7 +1197,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         p.H = H;
         if (S > 0) {
             p.Ks = (nm == 2) ? H : S;
-            p.MTs = ((nm == 2) ? S : H) / 128;
+            p.MTs = (nm == 2) ? S / 128 : H / 256;
             p.n_sgroups = (T + p.nt - 1) / p.nt;
             bool ok;
             if (nm == 2)

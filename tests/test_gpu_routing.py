@@ -56,7 +56,7 @@ def _check_calls(shape, L, T, calls, launches, w_tol=1e-6):
 
 
 @pytest.mark.parametrize("wl,T,calls,launches", [
-    ("decode_35b_a3b", 1, 16, 1),   # cluster decode kernel
+    ("decode_35b_a3b", 1, 16, 1),   # one-kernel decode path
     ("decode_35b_a3b", 4, 4, 1),
     ("verify8_zipf", 8, 4, 1),
     ("decode_h4096", 1, 8, 1),
