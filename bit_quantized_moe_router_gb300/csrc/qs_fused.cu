@@ -481,56 +481,105 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                 }
                 group_sync<kGTA>(2);
-                // order the entries by (expert, entry)
+                if (n_ent <= 32) {
+                    // one warp: entries ordered by (expert, entry) with shuffles, then the active
+                    // experts and each token's entries, without further group barriers
+                    if (gwarp == 0) {
+                        const bool act = lane < n_ent;
+                        const int e = act ? C.ids[lane] : 0x7fffffff;
+                        int rank = 0;
 #pragma unroll 1
-                for (int i = gtid; i < n_ent; i += kGTA) {
-                    const int e = C.ids[i];
-                    int rank = 0;
-#pragma unroll 8
-                    for (int j = 0; j < n_ent; j++) {
-                        const int f = C.ids[j];
-                        rank += (f < e) | ((f == e) & (j < i));
+                        for (int j = 0; j < n_ent; j++) {
+                            const int f = __shfl_sync(0xffffffffu, e, j);
+                            rank += (f < e) | ((f == e) & (j < lane));
+                        }
+                        if (act) {
+                            C.ent_sorted[rank] = lane;
+                            C.es[rank] = e;
+                            C.es_tok[rank] = lane / k;
+                        }
+                        __syncwarp();
+                        // lane: sorted position
+                        const int er = act ? C.es[lane] : -1;
+                        const int eprev = __shfl_up_sync(0xffffffffu, er, 1);
+                        const bool start = act && (lane == 0 || er != eprev);
+                        const unsigned bal = __ballot_sync(0xffffffffu, start);
+                        const int ai = __popc(bal & ((2u << lane) - 1u)) - 1;
+                        if (start) {
+                            C.act_e[ai] = er;
+                            C.act_begin[ai] = lane;
+                        }
+                        if (lane == n_ent - 1) {
+                            C.act_begin[ai + 1] = n_ent;
+                            C.n_active = ai + 1;
+                        }
+                        const int tr = act ? C.es_tok[lane] : -1;
+                        const unsigned same = __match_any_sync(0xffffffffu, tr);
+                        if (act) C.tok_sorted[tr * k + __popc(same & ((1u << lane) - 1u))] = lane;
+                        if (blockIdx.x == 0 && act) {  // the call's routing, for the caller to read back
+                            P.rec_ids[lane] = C.ids[lane];
+                            P.rec_p[lane] = C.p[lane];
+                        }
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int n_et = C.n_active * L.tpe;
+                            C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
+                            if (C.et_left == 0) publish(C, ctr_h, kPubH);  // no routed rows here
+                            mbar_arrive(&C.routed_bar);
+                        }
                     }
-                    C.ent_sorted[rank] = i;
-                    C.es[rank] = e;
-                    C.es_tok[rank] = i / k;
-                }
-                group_sync<kGTA>(2);
-                // active experts: a run start in es[] opens a new active expert
-                const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
-                const unsigned bal = __ballot_sync(0xffffffffu, start);
-                if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
-                group_sync<kGTA>(2);
-                if (gtid < n_ent) {
-                    int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+                } else {
+                    // order the entries by (expert, entry)
 #pragma unroll 1
-                    for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
-                    if (start) {
-                        C.act_e[a] = C.es[gtid];
-                        C.act_begin[a] = gtid;
-                    }
-                    if (gtid == n_ent - 1) {
-                        C.act_begin[a + 1] = n_ent;
-                        C.n_active = a + 1;
-                    }
-                    const int t = C.es_tok[gtid];
-                    int pos = 0;
-#pragma unroll 8
-                    for (int j = 0; j < gtid; j++) pos += C.es_tok[j] == t;
-                    C.tok_sorted[t * k + pos] = gtid;
-                }
-                if (blockIdx.x == 0) {  // the call's routing, for the caller to read back
                     for (int i = gtid; i < n_ent; i += kGTA) {
-                        P.rec_ids[i] = C.ids[i];
-                        P.rec_p[i] = C.p[i];
+                        const int e = C.ids[i];
+                        int rank = 0;
+#pragma unroll 8
+                        for (int j = 0; j < n_ent; j++) {
+                            const int f = C.ids[j];
+                            rank += (f < e) | ((f == e) & (j < i));
+                        }
+                        C.ent_sorted[rank] = i;
+                        C.es[rank] = e;
+                        C.es_tok[rank] = i / k;
                     }
-                }
-                group_sync<kGTA>(2);
-                if (gtid == 0) {
-                    const int n_et = C.n_active * L.tpe;
-                    C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
-                    if (C.et_left == 0) publish(C, ctr_h, kPubH);  // no routed rows here
-                    mbar_arrive(&C.routed_bar);
+                    group_sync<kGTA>(2);
+                    // active experts: a run start in es[] opens a new active expert
+                    const bool start = gtid < n_ent && (gtid == 0 || C.es[gtid] != C.es[gtid - 1]);
+                    const unsigned bal = __ballot_sync(0xffffffffu, start);
+                    if (lane == 0 && gwarp < 4) C.wcnt[gwarp] = __popc(bal);
+                    group_sync<kGTA>(2);
+                    if (gtid < n_ent) {
+                        int a = __popc(bal & ((2u << lane) - 1u)) - 1;
+#pragma unroll 1
+                        for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
+                        if (start) {
+                            C.act_e[a] = C.es[gtid];
+                            C.act_begin[a] = gtid;
+                        }
+                        if (gtid == n_ent - 1) {
+                            C.act_begin[a + 1] = n_ent;
+                            C.n_active = a + 1;
+                        }
+                        const int t = C.es_tok[gtid];
+                        int pos = 0;
+#pragma unroll 8
+                        for (int j = 0; j < gtid; j++) pos += C.es_tok[j] == t;
+                        C.tok_sorted[t * k + pos] = gtid;
+                    }
+                    if (blockIdx.x == 0) {  // the call's routing, for the caller to read back
+                        for (int i = gtid; i < n_ent; i += kGTA) {
+                            P.rec_ids[i] = C.ids[i];
+                            P.rec_p[i] = C.p[i];
+                        }
+                    }
+                    group_sync<kGTA>(2);
+                    if (gtid == 0) {
+                        const int n_et = C.n_active * L.tpe;
+                        C.et_left = owned_count(L.n_ind, L.n_ind + n_et, L.G, L.cta) * L.ept;
+                        if (C.et_left == 0) publish(C, ctr_h, kPubH);  // no routed rows here
+                        mbar_arrive(&C.routed_bar);
+                    }
                 }
             } else {
                 fail(C, status);
@@ -861,21 +910,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!(ok = got != 0 && warp_wait_mbar(C, &C.h_bar, 0))) break;
                 const float* hr = P.xh + (size_t)ent * F;
-                // lane: 8 consecutive values per 256; one pass for the scale, one to quantise
-                float m = 0.0f;
-#pragma unroll 2
-                for (int p = lane * 8; p < F; p += 256) {
-                    const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-                    m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-                }
-                m = warp_max(m);
-                const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
                 uint32_t* row = hqf + (size_t)ent * (F / 64) * kFragWords;
-#pragma unroll 2
-                for (int p = lane * 8; p < F; p += 256) {
-                    const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
-                    const float hv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                // lane: 8 consecutive values per 256; the max-abs scale, then int16 fragments
+                auto put8 = [&](int p, const float (&hv)[8], float inv) {
                     uint32_t wq[4];
                     int sum = 0;
 #pragma unroll
@@ -890,6 +927,46 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     frag_pos(p, word, half);
                     *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
                     if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
+                };
+                auto load8f = [&](int p, float (&hv)[8]) {
+                    const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
+                    hv[0] = a.x; hv[1] = a.y; hv[2] = a.z; hv[3] = a.w;
+                    hv[4] = b.x; hv[5] = b.y; hv[6] = b.z; hv[7] = b.w;
+                };
+                auto absmax8 = [](const float (&hv)[8], float m) {
+#pragma unroll
+                    for (int i = 0; i < 8; i++) m = fmaxf(m, fabsf(hv[i]));
+                    return m;
+                };
+                float m = 0.0f;
+                if (F <= 1024) {  // one pass over L2: the row stays in registers (F / 256 groups of 8)
+                    float hv[4][8];
+#pragma unroll
+                    for (int it = 0; it < 4; it++)
+                        if (it * 256 < F) load8f(lane * 8 + it * 256, hv[it]);
+#pragma unroll
+                    for (int it = 0; it < 4; it++)
+                        if (it * 256 < F) m = absmax8(hv[it], m);
+                    m = warp_max(m);
+                    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+#pragma unroll
+                    for (int it = 0; it < 4; it++)
+                        if (it * 256 < F) put8(lane * 8 + it * 256, hv[it], inv);
+                } else {  // two passes
+#pragma unroll 2
+                    for (int p = lane * 8; p < F; p += 256) {
+                        float hv[8];
+                        load8f(p, hv);
+                        m = absmax8(hv, m);
+                    }
+                    m = warp_max(m);
+                    const float inv = m > 0.0f ? 32767.0f / m : 0.0f;
+#pragma unroll 2
+                    for (int p = lane * 8; p < F; p += 256) {
+                        float hv[8];
+                        load8f(p, hv);
+                        put8(p, hv, inv);
+                    }
                 }
                 if (lane == 0) C.hscale[ent] = m * (1.0f / 32767.0f);
                 __syncwarp();

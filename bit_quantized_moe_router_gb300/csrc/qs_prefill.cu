@@ -151,6 +151,32 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     if (ok) (void)mbar_try_wait(bar, parity);
     return ok != 0;
 }
+// The same wait observed by lane 0 alone: the outcome reaches the warp through __syncwarp,
+// which also orders the other lanes' later memory accesses after lane 0's acquire.  For
+// warps whose lanes act on the phase only through lane 0 (the MMA issuer), or write what
+// the phase released only after the barrier.
+__device__ __forceinline__ bool lead_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* status,
+                                          uint32_t code = 0, uint32_t counter = 0) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+        const uint64_t t0 = global_timer_ns();
+        for (;;) {
+            if (mbar_try_wait_sleep(bar, parity, kSleepNs)) break;
+            if (*abort) {
+                ok = 0;
+                break;
+            }
+            if (global_timer_ns() - t0 > kWaitNs) {
+                *abort = 1;
+                note_timeout(status, code, counter);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
 // Abort flag as one value for the whole warp (lane 0's reading).
 __device__ __forceinline__ bool warp_aborted(volatile int* abort) {
     return __shfl_sync(0xffffffffu, *abort, 0) != 0;
@@ -460,7 +486,7 @@ __global__ void __launch_bounds__(256) pf_combine_kernel(const uint16_t* __restr
 
 constexpr int kMaxNA = 6;  // A stages (token rows, filled by TMA): as many as shared memory holds
 constexpr int kNW = 2;   // W stages (dequantised weight rows, or the shared expert's bf16 rows by TMA)
-constexpr int kNRv = 3;  // raw Q2_K slots
+constexpr int kMaxRv = 4;  // raw Q2_K slots: three column chunks, or four half-units of whole rows
 
 struct ExpertParams {
     CUtensorMap map_q;   // routed Q2_K rows, column mode: u8 [E][rows][rowbytes], box 112 x 128 x 1
@@ -482,6 +508,7 @@ struct ExpertParams {
     int nt;              // token-tile height (MMA M)
     int na;              // A stages
     int slot;            // raw slot bytes (kColSlot, or 128 whole rows)
+    int nrv;             // raw slots
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
@@ -497,7 +524,7 @@ struct ExpertParams {
 struct ExpertCtl {
     uint64_t afull[kMaxNA], aempty[kMaxNA];
     uint64_t wfull[kNW], wempty[kNW];
-    uint64_t rawfull[kNRv], rawfree[kNRv];
+    uint64_t rawfull[kMaxRv], rawfree[kMaxRv];
     uint64_t accfull[2], accempty[2], drain;
     uint32_t tmem;
     int abort;
@@ -602,11 +629,11 @@ template <int NM>
 __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __grid_constant__ ExpertParams p) {
     extern __shared__ uint8_t ex_smem_raw[];
     uint8_t* sm = align1024(ex_smem_raw);
-    const int NA = p.na, SLOT = p.slot;
+    const int NA = p.na, SLOT = p.slot, NRV = p.nrv;
     uint8_t* ast = sm;                       // NA x kABytes
     uint8_t* wst = ast + NA * kABytes;       // kNW x kWBytes
-    uint8_t* raw = wst + kNW * kWBytes;      // kNRv x SLOT
-    ExpertCtl* ctl = reinterpret_cast<ExpertCtl*>(raw + kNRv * SLOT);
+    uint8_t* raw = wst + kNW * kWBytes;      // NRV x SLOT
+    ExpertCtl* ctl = reinterpret_cast<ExpertCtl*>(raw + NRV * SLOT);
     ExpertTables tb;
     tb.prefix = reinterpret_cast<int*>(ctl + 1);
     tb.offs = tb.prefix + p.E + 1;
@@ -623,7 +650,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             mbar_init(&ctl->wfull[s], kDeqWarps);
             mbar_init(&ctl->wempty[s], 1);
         }
-        for (int r = 0; r < kNRv; r++) {
+        for (int r = 0; r < NRV; r++) {
             mbar_init(&ctl->rawfull[r], 1);
             mbar_init(&ctl->rawfree[r], kDeqWarps);
         }
@@ -686,7 +713,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 const int g = GW + kb, s = g % kNW;
                 uint32_t v[16];
                 dequant_half(scw, qw, c, jj, d, dm, v);
-                if (g >= kNW && !warp_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 3, g)) return false;
+                if (g >= kNW && !lead_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 3, g)) return false;
                 store_w_half(wst + s * kWBytes, r, jj, v);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
                 __syncwarp();
@@ -697,8 +724,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 const int nch = p.K / 256;
 #pragma unroll 1
                 for (int ch = 0; ch < nch; ch++, C++) {
-                    const int slot = C % kNRv;
-                    if (!warp_wait(&ctl->rawfull[slot], (C / kNRv) & 1, abort, p.status, 1, C)) return false;
+                    const int slot = C % NRV;
+                    if (!warp_wait(&ctl->rawfull[slot], (C / NRV) & 1, abort, p.status, 1, C)) return false;
                     // the block starts (84 ch) mod 16 bytes into the 112-byte row of the column box
                     const uint32_t row = smem_u32(raw + slot * SLOT) + (uint32_t)r * kColBox;
                     uint32_t win[24], w[21];
@@ -734,9 +761,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 }
             } else {
                 // tile mode: chunk C holds rows 0..127, chunk C + 1 rows 128..255, each whole
-                const int mine = C + (r >> 7), slot = mine % kNRv;
-                if (!warp_wait(&ctl->rawfull[C % kNRv], (C / kNRv) & 1, abort, p.status, 1, C) ||
-                    !warp_wait(&ctl->rawfull[(C + 1) % kNRv], ((C + 1) / kNRv) & 1, abort, p.status, 1, C + 1))
+                const int mine = C + (r >> 7), slot = mine % NRV;
+                if (!warp_wait(&ctl->rawfull[C % NRV], (C / NRV) & 1, abort, p.status, 1, C) ||
+                    !warp_wait(&ctl->rawfull[(C + 1) % NRV], ((C + 1) / NRV) & 1, abort, p.status, 1, C + 1))
                     return false;
                 const uint32_t row = smem_u32(raw + slot * SLOT) + (uint32_t)(r & 127) * p.rowbytes;
 #pragma unroll 1
@@ -753,8 +780,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 }
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&ctl->rawfree[C % kNRv]);
-                    mbar_arrive(&ctl->rawfree[(C + 1) % kNRv]);
+                    mbar_arrive(&ctl->rawfree[C % NRV]);
+                    mbar_arrive(&ctl->rawfree[(C + 1) % NRV]);
                 }
                 C += 2;
             }
@@ -858,18 +885,20 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         const uint32_t tmu = __shfl_sync(0xffffffffu, tbase, 0);
         const bool leader = lane == 0;
         int GA = 0, GW = 0, V = 0;
+        int sa = 0, sw = 0;             // current A and W stages
+        uint32_t pa = 0, pw = 0;        // ... and the parity of their fills
         for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
             if (warp_aborted(abort)) return false;
             const int KB = unit_kb(U, p);
             const int b = V & 1;
-            if (V >= 2 && !warp_wait(&ctl->accempty[b], ((V >> 1) - 1) & 1, abort, p.status, 5, V)) return false;
+            if (V >= 2 && !lead_wait(&ctl->accempty[b], ((V >> 1) - 1) & 1, abort, p.status, 5, V)) return false;
             tc::fence_after();
             const uint32_t id = tc::idesc(U.shared ? tc::kBF16 : tc::kF16, kNT, kWRows);
             const uint32_t d = tmu + b * 256;
             for (int kb = 0; kb < KB; kb++) {
-                const int ga = GA + kb, sa = ga % NA, gw = GW + kb, sw = gw % kNW;
-                if (!warp_wait(&ctl->afull[sa], (ga / NA) & 1, abort, p.status, 6, ga)) return false;
-                if (!warp_wait(&ctl->wfull[sw], (gw / kNW) & 1, abort, p.status, 8, gw)) return false;
+                const int ga = GA + kb, gw = GW + kb;
+                if (!lead_wait(&ctl->afull[sa], pa, abort, p.status, 6, ga)) return false;
+                if (!lead_wait(&ctl->wfull[sw], pw, abort, p.status, 8, gw)) return false;
                 tc::fence_after();
                 if (leader) {
                     const uint64_t ad = tc::sdesc_sw128(smem_u32(ast + sa * kABytes));
@@ -880,6 +909,14 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     tc::commit(&ctl->wempty[sw]);
                 }
                 __syncwarp();
+                if (++sa == NA) {  // next A and W stages and their phases
+                    sa = 0;
+                    pa ^= 1;
+                }
+                if (++sw == kNW) {
+                    sw = 0;
+                    pw ^= 1;
+                }
             }
             if (leader) tc::commit(&ctl->accfull[b]);
             __syncwarp();
@@ -926,8 +963,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 } else if (do_raw) {
                     const int nch = unit_nch(U, p);
                     for (int ch = 0; ch < nch; ch++, C++) {
-                        const int slot = C % kNRv;
-                        if (C >= kNRv && !thread_wait(&ctl->rawfree[slot], ((C / kNRv) - 1) & 1, abort, p.status, 9, C))
+                        const int slot = C % NRV;
+                        if (C >= NRV && !thread_wait(&ctl->rawfree[slot], ((C / NRV) - 1) & 1, abort, p.status, 9, C))
                             return false;
                         uint8_t* sl = raw + slot * SLOT;
                         uint64_t* bar = &ctl->rawfull[slot];
@@ -968,9 +1005,9 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 return true;
             });
             if (*abort) {  // let issued copies land before the CTA exits
-                for (int i = 1; do_raw && i <= kNRv && i <= C; i++) {
+                for (int i = 1; do_raw && i <= NRV && i <= C; i++) {
                     const int c = C - i;
-                    (void)mbar_wait(&ctl->rawfull[c % kNRv], (c / kNRv) & 1, 1000000ull);
+                    (void)mbar_wait(&ctl->rawfull[c % NRV], (c / NRV) & 1, 1000000ull);
                 }
                 for (int s = 0; do_raw && s < kNW; s++)
                     if (wt_last[s] >= 0) (void)mbar_wait(&ctl->wfull[s], (wt_last[s] / kNW) & 1, 1000000ull);
@@ -1066,8 +1103,8 @@ cudaError_t pf_facts(PfFacts** out) {
 }
 
 // Dynamic shared memory of an expert kernel with na A stages and raw slots of `slot` bytes.
-size_t expert_smem(int E, int na, int slot) {
-    return 1024 + (size_t)na * kABytes + (size_t)kNW * kWBytes + (size_t)kNRv * slot + sizeof(ExpertCtl) +
+size_t expert_smem(int E, int na, int slot, int nrv) {
+    return 1024 + (size_t)na * kABytes + (size_t)kNW * kWBytes + (size_t)nrv * slot + sizeof(ExpertCtl) +
            4 * (3 * (size_t)E + 1);
 }
 // Raw slot bytes for contraction length K (a column chunk, or 128 whole rows).
@@ -1076,9 +1113,12 @@ int slot_for(int K) {
     return raw_mode_for(K) == kRawColumn ? kColSlot : 128 * rowbytes;
 }
 // A stages that fit beside the rest (0: the kernel does not fit at all).
-int stages_for(int E, int slot, size_t smem_optin) {
+// Raw slots for contraction length K: a tile-mode unit holds two slots for all of its slices,
+// so four let the next unit's rows land meanwhile.
+int nrv_for(int K) { return raw_mode_for(K) == kRawColumn ? 3 : 4; }
+int stages_for(int E, int K, size_t smem_optin) {
     int na = kMaxNA;
-    while (na >= 2 && expert_smem(E, na, slot) > smem_optin) na--;
+    while (na >= 2 && expert_smem(E, na, slot_for(K), nrv_for(K)) > smem_optin) na--;
     return na >= 2 ? na : 0;
 }
 size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCtl); }
@@ -1086,7 +1126,7 @@ size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCt
 // Launch one expert kernel, one CTA per SM.
 template <int NM>
 cudaError_t launch_expert(ExpertParams& p, int n_sm, int E, cudaStream_t st) {
-    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem(E, p.na, p.slot), st>>>(p);
+    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem(E, p.na, p.slot, p.nrv), st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1120,8 +1160,8 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
     const int H = s.hidden, E = s.n_experts, k = s.top_k, F = s.expert_ffn;
     const int S = (sg != nullptr) ? s.shared_ffn : 0;
     const int n = T * k;
-    const int na2 = stages_for(E, slot_for(H), (size_t)f->smem_optin);
-    const int na1 = stages_for(E, slot_for(F), (size_t)f->smem_optin);
+    const int na2 = stages_for(E, H, (size_t)f->smem_optin);
+    const int na1 = stages_for(E, F, (size_t)f->smem_optin);
     if (na2 == 0 || na1 == 0 || (size_t)f->smem_optin < router_smem()) return cudaErrorNotSupported;
     if (!get_encode()) return cudaErrorNotSupported;
     if (!f->attr_set) {
@@ -1169,6 +1209,7 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         const int rowbytes = K / 256 * 84;
         p.raw_mode = raw_mode_for(K);
         p.slot = slot_for(K);
+        p.nrv = nrv_for(K);
         p.na = (nm == 2) ? na2 : na1;
         p.rowbytes = rowbytes;
         p.experts = experts;
