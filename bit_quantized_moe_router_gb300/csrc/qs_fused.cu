@@ -70,7 +70,8 @@ constexpr int kStageBytes = 21504;       // 2 x 128 Q2_K row-blocks of 84 B
 constexpr int kMaxStages = 12;
 constexpr int kMaxEnt = 128;             // T * k
 constexpr int kMaxT = kFusedMaxT;
-constexpr int kMaxCand = 512;            // tokens x 32-logit chunks x min(k, 32) the plan admits
+constexpr int kMaxCand = 512;            // tokens x 32-logit chunks x min(k, 32) this kernel takes; larger
+                                         // calls (12-16 tokens of 256 experts) ran faster on the tensor cores
 constexpr int kMaxRD = 16;
 
 struct FusedParams {
@@ -707,6 +708,39 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int n_stage_tasks = (S > 0 ? 1 : 0) + n_ent;
         const int q_et = own_et * L.ept;              // pool: routed gate/up tasks
         const int q_all = q_et + n_stage_tasks + own_dg * P.RD;
+        // ---------------------------------------------------------- routed gate/up rows
+        // Tasks q = warp, warp + kCW, ... below q_et.  A lane owns chunk c0 + i * cstep (i < nch) of
+        // row rl of the task; its chunks are one stream, loaded one item ahead of the one computed
+        // (so the next task's rows are in flight while this task is reduced and stored).  Per entry
+        // of the expert, the chunk dots are added in chunk order, then across lanes.
+        int q = warp;
+        if (ok && q < q_et) {
+            if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) fail(C, status);
+        }
+        const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
+        const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
+        const int cstep = L.cpr >= 32 ? 32 : L.cpr;
+        const int nch = L.cpr / cstep;
+        const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
+        const int g0 = first_owned(L.n_ind, L.G, L.cta);
+        // first byte of this lane's gate row of task qq (the up row is F rows further)
+        auto task_row = [&](int qq) -> const uint8_t* {
+            const int m = qq / L.ept, rt = qq % L.ept;
+            const int idx = g0 + m * L.G - L.n_ind;
+            const int a = idx / L.tpe, tt = idx % L.tpe;
+            return P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw + rl) * L.rowH;
+        };
+        const int64_t up_off = (int64_t)P.F * L.rowH;
+        // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
+        const bool hoist = MAXT == 1 && nch == 1;
+        XFrag fx;
+        Q2Chunk pg, pu;  // the next item's words, in flight
+        if (ok && q < q_et) {  // the first task's rows, requested before the L2 requests below
+            if (hoist) load_xfrag_f(xqf + (size_t)c0 * kFragWords, fx);
+            const uint8_t* gr = task_row(q);
+            load_q2chunk_global(gr + (c0 >> 2) * kBlockBytes, c0 & 3, pg);
+            load_q2chunk_global(gr + up_off + (c0 >> 2) * kBlockBytes, c0 & 3, pu);
+        }
         // every routed gate/up row and every routed down row this CTA will read, requested into L2
         // at once, one 128-byte line per consumer thread at a time (gate/up lines first, in task order)
         {
@@ -739,40 +773,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
             }
         }
-        // ---------------------------------------------------------- routed gate/up rows
-        // Tasks q = warp, warp + kCW, ... below q_et.  A lane owns chunk c0 + i * cstep (i < nch) of
-        // row rl of the task; its chunks are one stream, loaded one item ahead of the one computed
-        // (so the next task's rows are in flight while this task is reduced and stored).  Per entry
-        // of the expert, the chunk dots are added in chunk order, then across lanes.
-        int q = warp;
         if (ok && q < q_et) {
-            if (!(ok = warp_wait_mbar(C, &C.xq_bar, 0))) fail(C, status);
-        }
-        if (ok && q < q_et) {
-            const int rl = L.cpr >= 32 ? 0 : lane / L.cpr;
-            const int c0 = L.cpr >= 32 ? lane : lane % L.cpr;
-            const int cstep = L.cpr >= 32 ? 32 : L.cpr;
-            const int nch = L.cpr / cstep;
-            const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
-            const int g0 = first_owned(L.n_ind, L.G, L.cta);
-            // first byte of this lane's gate row of task qq (the up row is F rows further)
-            auto task_row = [&](int qq) -> const uint8_t* {
-                const int m = qq / L.ept, rt = qq % L.ept;
-                const int idx = g0 + m * L.G - L.n_ind;
-                const int a = idx / L.tpe, tt = idx % L.tpe;
-                return P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw + rl) * L.rowH;
-            };
-            const int64_t up_off = (int64_t)P.F * L.rowH;
-            // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
-            const bool hoist = MAXT == 1 && nch == 1;
-            XFrag fx;
-            if (hoist) load_xfrag_f(xqf + (size_t)c0 * kFragWords, fx);
-            Q2Chunk pg, pu;  // the next item's words, in flight
-            {
-                const uint8_t* gr = task_row(q);
-                load_q2chunk_global(gr + (c0 >> 2) * kBlockBytes, c0 & 3, pg);
-                load_q2chunk_global(gr + up_off + (c0 >> 2) * kBlockBytes, c0 & 3, pu);
-            }
 #pragma unroll 1
             for (; q < q_et; q += kCW) {
                 const int m = q / L.ept, rt = q % L.ept;
@@ -939,7 +940,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     return m;
                 };
                 float m = 0.0f;
-                if (F <= 1024) {  // one pass over L2: the row stays in registers (F / 256 groups of 8)
+                if (MAXT > 1 && F <= 1024) {  // one pass over L2: the row stays in registers (measured: one
+                                              // token is faster with two passes)
                     float hv[4][8];
 #pragma unroll
                     for (int it = 0; it < 4; it++)

@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(256) pf_combine_kernel(const uint16_t* __restr
 // ================================================================== grouped expert GEMMs
 
 constexpr int kMaxNA = 6;  // A stages (token rows, filled by TMA): as many as shared memory holds
-constexpr int kNW = 2;   // W stages (dequantised weight rows, or the shared expert's bf16 rows by TMA)
+constexpr int kMaxNW = 3;  // W stages (dequantised weight rows, or the shared expert's bf16 rows by TMA)
 constexpr int kMaxRv = 4;  // raw Q2_K slots: three column chunks, or four half-units of whole rows
 
 struct ExpertParams {
@@ -509,6 +509,7 @@ struct ExpertParams {
     int na;              // A stages
     int slot;            // raw slot bytes (kColSlot, or 128 whole rows)
     int nrv;             // raw slots
+    int nw;              // W stages
     const int32_t* counts;
     const int32_t* offsets;
     const int32_t* perm;
@@ -523,7 +524,7 @@ struct ExpertParams {
 
 struct ExpertCtl {
     uint64_t afull[kMaxNA], aempty[kMaxNA];
-    uint64_t wfull[kNW], wempty[kNW];
+    uint64_t wfull[kMaxNW], wempty[kMaxNW];
     uint64_t rawfull[kMaxRv], rawfree[kMaxRv];
     uint64_t accfull[2], accempty[2], drain;
     uint32_t tmem;
@@ -609,6 +610,18 @@ __device__ __forceinline__ void store_w_half(uint8_t* wst, int r, int jj, const 
     }
 }
 
+// W stage of fill g and how many fills of that stage came before (NW is 2 or 3: divisions by
+// constants).
+__device__ __forceinline__ void w_stage(int g, int NW, int& s, int& fill) {
+    if (NW == 2) {
+        s = g & 1;
+        fill = g >> 1;
+    } else {
+        s = g % 3;
+        fill = g / 3;
+    }
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -629,10 +642,10 @@ template <int NM>
 __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __grid_constant__ ExpertParams p) {
     extern __shared__ uint8_t ex_smem_raw[];
     uint8_t* sm = align1024(ex_smem_raw);
-    const int NA = p.na, SLOT = p.slot, NRV = p.nrv;
+    const int NA = p.na, SLOT = p.slot, NRV = p.nrv, NW = p.nw;
     uint8_t* ast = sm;                       // NA x kABytes
-    uint8_t* wst = ast + NA * kABytes;       // kNW x kWBytes
-    uint8_t* raw = wst + kNW * kWBytes;      // NRV x SLOT
+    uint8_t* wst = ast + NA * kABytes;       // NW x kWBytes
+    uint8_t* raw = wst + NW * kWBytes;      // NRV x SLOT
     ExpertCtl* ctl = reinterpret_cast<ExpertCtl*>(raw + NRV * SLOT);
     ExpertTables tb;
     tb.prefix = reinterpret_cast<int*>(ctl + 1);
@@ -646,7 +659,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             mbar_init(&ctl->afull[s], 1);
             mbar_init(&ctl->aempty[s], 1);
         }
-        for (int s = 0; s < kNW; s++) {
+        for (int s = 0; s < NW; s++) {
             mbar_init(&ctl->wfull[s], kDeqWarps);
             mbar_init(&ctl->wempty[s], 1);
         }
@@ -710,10 +723,12 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             }
             // one 64-wide slice: weights of row r from the block words w[] -> W stage (GW + kb)
             auto slice = [&](int kb, int c, uint32_t scw, const uint32_t (&qw)[8], float d, float dm) -> bool {
-                const int g = GW + kb, s = g % kNW;
+                const int g = GW + kb;
+                int s, fill;
+                w_stage(g, NW, s, fill);
                 uint32_t v[16];
                 dequant_half(scw, qw, c, jj, d, dm, v);
-                if (g >= kNW && !lead_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 3, g)) return false;
+                if (fill > 0 && !lead_wait(&ctl->wempty[s], (fill - 1) & 1, abort, p.status, 3, g)) return false;
                 store_w_half(wst + s * kWBytes, r, jj, v);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
                 __syncwarp();
@@ -913,7 +928,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     sa = 0;
                     pa ^= 1;
                 }
-                if (++sw == kNW) {
+                if (++sw == NW) {
                     sw = 0;
                     pw ^= 1;
                 }
@@ -936,16 +951,18 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
         const bool do_raw = (warp == kWarpRaw), do_a = (warp == kWarpA);
         if (lane == 0) {
             int C = 0, GW = 0, GA = 0;
-            int wt_last[kNW];  // per W stage, the last fill this thread issued (-1: none)
-            for (int i = 0; i < kNW; i++) wt_last[i] = -1;
+            int wt_last[kMaxNW];  // per W stage, the last fill this thread issued (-1: none)
+            for (int i = 0; i < NW; i++) wt_last[i] = -1;
             for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
                 if (*abort) return false;
                 const int KB = unit_kb(U, p);
                 if (do_raw && U.shared) {
                     // the shared expert's bf16 rows are the W operand as they land: two 128-row boxes
                     for (int kb = 0; kb < KB; kb++) {
-                        const int g = GW + kb, s = g % kNW;
-                        if (g >= kNW && !thread_wait(&ctl->wempty[s], ((g / kNW) - 1) & 1, abort, p.status, 10, g))
+                        const int g = GW + kb;
+                        int s, fill;
+                        w_stage(g, NW, s, fill);
+                        if (fill > 0 && !thread_wait(&ctl->wempty[s], (fill - 1) & 1, abort, p.status, 10, g))
                             return false;
                         uint8_t* w = wst + s * kWBytes;
                         uint64_t* bar = &ctl->wfull[s];
@@ -1009,8 +1026,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     const int c = C - i;
                     (void)mbar_wait(&ctl->rawfull[c % NRV], (c / NRV) & 1, 1000000ull);
                 }
-                for (int s = 0; do_raw && s < kNW; s++)
-                    if (wt_last[s] >= 0) (void)mbar_wait(&ctl->wfull[s], (wt_last[s] / kNW) & 1, 1000000ull);
+                for (int s = 0; do_raw && s < NW; s++)
+                    if (wt_last[s] >= 0) (void)mbar_wait(&ctl->wfull[s], (wt_last[s] / NW) & 1, 1000000ull);
                 for (int i = 1; do_a && i <= NA && i <= GA; i++) {
                     const int c = GA - i;
                     (void)mbar_wait(&ctl->afull[c % NA], (c / NA) & 1, 1000000ull);
@@ -1103,8 +1120,8 @@ cudaError_t pf_facts(PfFacts** out) {
 }
 
 // Dynamic shared memory of an expert kernel with na A stages and raw slots of `slot` bytes.
-size_t expert_smem(int E, int na, int slot, int nrv) {
-    return 1024 + (size_t)na * kABytes + (size_t)kNW * kWBytes + (size_t)nrv * slot + sizeof(ExpertCtl) +
+size_t expert_smem(int E, int na, int slot, int nrv, int nw) {
+    return 1024 + (size_t)na * kABytes + (size_t)nw * kWBytes + (size_t)nrv * slot + sizeof(ExpertCtl) +
            4 * (3 * (size_t)E + 1);
 }
 // Raw slot bytes for contraction length K (a column chunk, or 128 whole rows).
@@ -1113,20 +1130,25 @@ int slot_for(int K) {
     return raw_mode_for(K) == kRawColumn ? kColSlot : 128 * rowbytes;
 }
 // A stages that fit beside the rest (0: the kernel does not fit at all).
-// Raw slots for contraction length K: a tile-mode unit holds two slots for all of its slices,
-// so four let the next unit's rows land meanwhile.
-int nrv_for(int K) { return raw_mode_for(K) == kRawColumn ? 3 : 4; }
-int stages_for(int E, int K, size_t smem_optin) {
-    int na = kMaxNA;
-    while (na >= 2 && expert_smem(E, na, slot_for(K), nrv_for(K)) > smem_optin) na--;
-    return na >= 2 ? na : 0;
+struct StagePlan {
+    int na, nw, nrv;  // A stages, W stages, raw slots (0: the kernel does not fit)
+};
+// Stages for contraction length K: three W stages, the raw slots (two column chunks, or four
+// halves of whole-row units), and as many A stages (two at least) as fit beside them.  Of
+// the plans measured at 2048 and 512 tokens of the 35B-A3B layer (W stages 2 or 3, column
+// raw slots 2 or 3) this one was fastest.
+StagePlan stages_for(int E, int K, size_t smem_optin) {
+    StagePlan sp{kMaxNA, 3, raw_mode_for(K) == kRawColumn ? 2 : 4};
+    while (sp.na >= 2 && expert_smem(E, sp.na, slot_for(K), sp.nrv, sp.nw) > smem_optin) sp.na--;
+    if (sp.na < 2) sp.na = 0;
+    return sp;
 }
 size_t router_smem() { return 1024 + kRouterStages * 4 * 16384 + sizeof(RouterCtl); }
 
 // Launch one expert kernel, one CTA per SM.
 template <int NM>
 cudaError_t launch_expert(ExpertParams& p, int n_sm, int E, cudaStream_t st) {
-    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem(E, p.na, p.slot, p.nrv), st>>>(p);
+    pf_expert_kernel<NM><<<n_sm, kExpertThreads, expert_smem(E, p.na, p.slot, p.nrv, p.nw), st>>>(p);
     return cudaGetLastError();
 }
 
@@ -1160,9 +1182,9 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
     const int H = s.hidden, E = s.n_experts, k = s.top_k, F = s.expert_ffn;
     const int S = (sg != nullptr) ? s.shared_ffn : 0;
     const int n = T * k;
-    const int na2 = stages_for(E, H, (size_t)f->smem_optin);
-    const int na1 = stages_for(E, F, (size_t)f->smem_optin);
-    if (na2 == 0 || na1 == 0 || (size_t)f->smem_optin < router_smem()) return cudaErrorNotSupported;
+    const StagePlan sp2 = stages_for(E, H, (size_t)f->smem_optin);
+    const StagePlan sp1 = stages_for(E, F, (size_t)f->smem_optin);
+    if (sp2.na == 0 || sp1.na == 0 || (size_t)f->smem_optin < router_smem()) return cudaErrorNotSupported;
     if (!get_encode()) return cudaErrorNotSupported;
     if (!f->attr_set) {
         if ((e = cudaFuncSetAttribute(pf_router_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1209,8 +1231,10 @@ cudaError_t launch_prefill(const qs_moe_shape& s, const void* x, const float* Wr
         const int rowbytes = K / 256 * 84;
         p.raw_mode = raw_mode_for(K);
         p.slot = slot_for(K);
-        p.nrv = nrv_for(K);
-        p.na = (nm == 2) ? na2 : na1;
+        const StagePlan& sp = (nm == 2) ? sp2 : sp1;
+        p.na = sp.na;
+        p.nw = sp.nw;
+        p.nrv = sp.nrv;
         p.rowbytes = rowbytes;
         p.experts = experts;
         p.stride = stride;
