@@ -70,14 +70,15 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the oracle CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--format", default="q2k", choices=["q2k", "q4k"],
-                    help="routed expert format: Q2_K (the workloads' format) or Q4_K (per-step kernels)")
+                    help="routed expert format: Q2_K (the workloads' format) or Q4_K")
     ap.add_argument("--steer", type=float, default=0.0,
                     help="directional steering of every output row with this scale (0: off)")
     return ap.parse_args()
 
 
 KERNEL_SOURCES = ("bit_quantized_moe_router_gb300/csrc/qs_fused.cu", "bit_quantized_moe_router_gb300/csrc/qs_q2k.cuh",
-                  "bit_quantized_moe_router_gb300/csrc/qs_common.cuh")
+                  "bit_quantized_moe_router_gb300/csrc/qs_common.cuh", "bit_quantized_moe_router_gb300/csrc/qs_fmt.cuh",
+                  "bit_quantized_moe_router_gb300/csrc/qs_warp.cuh")
 
 
 def recorded_traffic(workload):
@@ -409,7 +410,7 @@ def run_ours(args, w, T):
     H = sh.hidden
     shape = qm.make_shape(sh.hidden, sh.n_experts, sh.top_k, sh.expert_ffn, sh.shared_ffn, sh.x_dtype)
     launches_per_step = qm.qs_moe_ffn_launches(shape, T, True) if args.format == "q2k" else \
-        (6 if sh.shared_ffn > 0 else 4)   # Q4_K: shared gate/up, route, group, gate/up, down, shared down
+        qm.qs_moe_ffn_q4k_launches(shape, T, True)
     if launches_per_step < 1:
         raise SystemExit(f"qs_moe_ffn_launches failed ({launches_per_step})")
     layer_launches = launches_per_step
@@ -641,19 +642,21 @@ def run_ours(args, w, T):
                 "algorithmic_flops_per_launch": flops, "traffic": None}
     else:
         roof = {"bound": "hbm",
-                "kernel": ("fused_decode_kernel" if layer_launches == 1 else "qs_moe_ffn (whole layer)")
-                if args.format == "q2k" else "qs_moe_ffn_q4k (whole layer, %d kernels)" % layer_launches,
+                "kernel": ("fused_decode_kernel" + (" (Q4_K experts)" if args.format == "q4k" else "")
+                           if layer_launches == 1 else
+                           "qs_moe_ffn (whole layer)" if args.format == "q2k" else
+                           "qs_moe_ffn_q4k (whole layer, %d kernels)" % layer_launches),
                 "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if pk else "fallback 6800 GB/s",
                 "algorithmic_bytes_per_launch": algo_bytes,
                 "traffic": recorded_traffic(w.name) if layer_launches == 1 and T == w.tokens[0] and not args.steer
-                else None}
+                and args.format == "q2k" else None}
     line = {
         "metric": metric_name(T) + (" [Q4_K experts]" if args.format == "q4k" else ""),
         "value": value, "unit": "tokens/s", "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": mean_step_s * 1e3, "us_per_layer": mean_step_s * 1e6,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("q4k-f32" if args.format == "q4k" else
+        "dtype": (("q4k-int16dot-f32" if layer_launches == 1 else "q4k-f32") if args.format == "q4k" else
                   "q2k-int16dot-f32" if roof["bound"] == "hbm" else "q2k-dequant-f16-mma-f32"), "data": "synthetic",
         "config": config_of(w, T, args),
         "achieved_gbs_all_bytes": achieved, "achieved_gbs_q2k_bytes": q2k_bytes / mean_step_s / 1e9,

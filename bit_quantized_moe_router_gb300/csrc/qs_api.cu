@@ -383,6 +383,16 @@ int qs_moe_ffn_launches(const qs_moe_shape* shape, int n_tokens, int has_shared)
     return eff.shared_ffn > 0 ? 5 : 4;
 }
 
+int qs_moe_ffn_q4k_launches(const qs_moe_shape* shape, int n_tokens, int has_shared) {
+    if (!shape_ok(shape) || n_tokens < 1) return 0;
+    qs_moe_shape eff = *shape;
+    if (!has_shared) eff.shared_ffn = 0;
+    cudaError_t e;
+    if (fused_decode_supported(eff, n_tokens, &e)) return 1;
+    if (e != cudaSuccess) return -(int)e;
+    return eff.shared_ffn > 0 ? 6 : 4;
+}
+
 int qs_q2k_quantize(const float* w, int64_t n_rows, int64_t K, void* out, void* stream) {
     if (!w || !out || n_rows < 1 || K < 256 || K % 256 || !aligned16(w) || ((uintptr_t)out & 3u))
         return QS_ERR_INVALID;
@@ -410,6 +420,18 @@ int qs_moe_ffn_q4k(const qs_moe_shape* shape, const void* x, const float* router
     int32_t* ids = ws_at<int32_t>(workspace, L.ids);
     float* pw = ws_at<float>(workspace, L.pw);
     cudaError_t e;
+    {  // one kernel (the persistent decode kernel with Q4_K routed rows) where it plans the call
+        qs_moe_shape eff = *shape;
+        if (!has_shared) eff.shared_ffn = 0;
+        e = launch_fused_decode(eff, x, router_w, router_bias, blocks, experts->expert_stride,
+                                has_shared ? (const uint16_t*)shared->w_gate : nullptr,
+                                has_shared ? (const uint16_t*)shared->w_up : nullptr,
+                                has_shared ? (const uint16_t*)shared->w_down : nullptr,
+                                has_shared ? (const uint16_t*)shared->w_gate_sig : nullptr, n_tokens, out, workspace, L,
+                                st, false, 1);
+        if (e == cudaSuccess) return QS_OK;
+        if (e != cudaErrorNotSupported) return cuda_fail(e);
+    }
     if (has_shared) {
         e = launch_shared_gateup(*shape, x, (const uint16_t*)shared->w_gate, (const uint16_t*)shared->w_up,
                                  (const uint16_t*)shared->w_gate_sig, n_tokens, hs, gate, st);

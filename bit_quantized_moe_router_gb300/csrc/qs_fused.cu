@@ -51,6 +51,7 @@
 #include "qs_common.cuh"
 #include "qs_internal.h"
 #include "qs_q2k.cuh"
+#include "qs_fmt.cuh"
 #include "qs_warp.cuh"
 
 #include <algorithm>
@@ -193,7 +194,7 @@ __device__ __forceinline__ int owned_count(int lo, int hi, int G, int cta) {
     return f < hi ? (hi - 1 - f) / G + 1 : 0;
 }
 
-__device__ __forceinline__ Plan make_plan(const FusedParams& P) {
+__device__ __forceinline__ Plan make_plan(const FusedParams& P, int block_bytes) {
     Plan L;
     L.G = gridDim.x;
     L.cta = blockIdx.x;
@@ -202,8 +203,8 @@ __device__ __forceinline__ Plan make_plan(const FusedParams& P) {
     L.n_ind = L.n_rt + L.n_st;
     L.tpe = P.F / P.R;
     L.n_dg = P.H / P.RD;
-    L.rowH = P.H / kBlockWeights * kBlockBytes;
-    L.rowF = P.F / kBlockWeights * kBlockBytes;
+    L.rowH = P.H / kBlockWeights * block_bytes;
+    L.rowF = P.F / kBlockWeights * block_bytes;
     L.own_rt = owned_count(0, L.n_rt, L.G, L.cta);
     L.own_st = owned_count(L.n_rt, L.n_ind, L.G, L.cta);
     L.cpr = 4 * (P.H / kBlockWeights);
@@ -294,7 +295,7 @@ __device__ __forceinline__ bool producer_slot(FusedCtl& C, int seq, int ns) {
 }
 
 __device__ void producer(const FusedParams& P, FusedCtl& C, uint8_t* data) {
-    const Plan L = make_plan(P);
+    const Plan L = make_plan(P, kBlockBytes);  // the tile counts only (no routed row sizes)
     const int lane = threadIdx.x & 31;
     const int ns = P.nstages;
     uint8_t* stages = data + P.off_stages;
@@ -365,8 +366,10 @@ done:
 
 // ------------------------------------------------------------------ the kernel
 
-template <int MAXT>
+// FMT: the routed experts' weight format (kFmtQ2K, kFmtQ4K).
+template <int MAXT, int FMT>
 __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const FusedParams P) {
+    using FO = FmtOps<FMT>;
     extern __shared__ __align__(128) uint8_t smem[];
     FusedCtl& C = *reinterpret_cast<FusedCtl*>(smem);
     uint8_t* data = smem + (sizeof(FusedCtl) + 127) / 128 * 128;
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         // every earlier call has left (the wait above), none of this call can leave before this
         // CTA publishes its logits: the exit count is an exact multiple of gridDim here
         if (tid == 0) C.target = (ld_relaxed_u64(ctr_exit) / gridDim.x + 1) * gridDim.x;
-        const Plan L = make_plan(P);
+        const Plan L = make_plan(P, FO::kBlock);
         const int gtid = warp < kGWA ? tid : tid - kGTA, gwarp = warp < kGWA ? warp : warp - kGWA;
         if (P.x_sys) {  // x from mapped host memory: every load in flight, then the stores
             const int nv = P.T * P.H * (x_f32 ? 4 : 2) / 16;
@@ -651,14 +654,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
                         sum += a0 + a1;
                     }
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                    if (live) {
-                        int word, half;
-                        frag_pos(p, word, half);
-                        uint32_t* row = xqf + (size_t)t * (H / 64) * kFragWords;
-                        *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                        if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
-                    }
+                    FO::put8(xqf + (size_t)t * (H / 64) * kFragWords, p, wq, sum, live);
                 }
                 group_sync<kGTB>(3);
                 if (gtid == 0) mbar_arrive(&C.xq_bar);
@@ -732,14 +728,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         };
         const int64_t up_off = (int64_t)P.F * L.rowH;
         // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
-        const bool hoist = MAXT == 1 && nch == 1;
-        XFrag fx;
-        Q2Chunk pg, pu;  // the next item's words, in flight
+        const bool hoist = FMT == kFmtQ2K && MAXT == 1 && nch == 1;
+        typename FO::Frag fx;
+        typename FO::Chunk pg, pu;  // the next item's words, in flight
         if (ok && q < q_et) {  // the first task's rows, requested before the L2 requests below
-            if (hoist) load_xfrag_f(xqf + (size_t)c0 * kFragWords, fx);
+            if (hoist) FO::load_frag(xqf + (size_t)c0 * kFragWords, fx);
             const uint8_t* gr = task_row(q);
-            load_q2chunk_global(gr + (c0 >> 2) * kBlockBytes, c0 & 3, pg);
-            load_q2chunk_global(gr + up_off + (c0 >> 2) * kBlockBytes, c0 & 3, pu);
+            FO::load(gr + (c0 >> 2) * FO::kBlock, c0 & 3, pg);
+            FO::load(gr + up_off + (c0 >> 2) * FO::kBlock, c0 & 3, pu);
         }
         // every routed gate/up row and every routed down row this CTA will read, requested into L2
         // at once, one 128-byte line per consumer thread at a time (gate/up lines first, in task order)
@@ -787,21 +783,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 1
                 for (int i = 0; i < nch; i++) {
                     const int c = c0 + i * cstep;
-                    const Q2Chunk gc = pg, uc = pu;
+                    const typename FO::Chunk gc = pg, uc = pu;
                     // request the next item: this task's next chunk, or the next task's first
                     if (i + 1 < nch) {
-                        const uint8_t* gr = task_row(q) + ((c + cstep) >> 2) * kBlockBytes;
-                        load_q2chunk_global(gr, (c + cstep) & 3, pg);
-                        load_q2chunk_global(gr + up_off, (c + cstep) & 3, pu);
+                        const uint8_t* gr = task_row(q) + ((c + cstep) >> 2) * FO::kBlock;
+                        FO::load(gr, (c + cstep) & 3, pg);
+                        FO::load(gr + up_off, (c + cstep) & 3, pu);
                     } else if (q + kCW < q_et) {
-                        const uint8_t* gr = task_row(q + kCW) + (c0 >> 2) * kBlockBytes;
-                        load_q2chunk_global(gr, c0 & 3, pg);
-                        load_q2chunk_global(gr + up_off, c0 & 3, pu);
+                        const uint8_t* gr = task_row(q + kCW) + (c0 >> 2) * FO::kBlock;
+                        FO::load(gr, c0 & 3, pg);
+                        FO::load(gr + up_off, c0 & 3, pu);
                     }
                     if (hoist) {
                         if (ne > 0) {
-                            gacc[0] += q2k_chunk_dot(gc, c & 3, fx);
-                            uacc[0] += q2k_chunk_dot(uc, c & 3, fx);
+                            gacc[0] += FO::dot(gc, c & 3, fx);
+                            uacc[0] += FO::dot(uc, c & 3, fx);
                         }
                     } else {
 #pragma unroll
@@ -809,7 +805,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                             if (e < ne) {
                                 const int t = C.ent_sorted[j0 + e] / k;
                                 float dg, du;
-                                q2k_chunk_dot2_f(gc, uc, c & 3, xqf + ((size_t)t * (H / 64) + c) * kFragWords, dg, du);
+                                FO::dot2(gc, uc, c & 3, xqf + ((size_t)t * (H / 64) + c) * kFragWords, dg, du);
                                 gacc[e] += dg;
                                 uacc[e] += du;
                             }
@@ -853,14 +849,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int np = (na + L.epp - 1) / L.epp;
         const int f_dg = first_owned(lo_dg, L.G, L.cta);
         float* pb = pbuf + warp * kMaxEnt;
-        const uint8_t* dbase = P.experts + 2ll * P.F * L.rowH + (dc0 >> 2) * kBlockBytes;
+        const uint8_t* dbase = P.experts + 2ll * P.F * L.rowH + (dc0 >> 2) * FO::kBlock;
         auto drow = [&](int qq) -> int {  // output row of down task qq
             const int dq = qq - q_et - n_stage_tasks;
             return (f_dg + (dq / P.RD) * L.G - lo_dg) * P.RD + dq % P.RD;
         };
         int iq = q, ip = 0;  // next item to request
         while (iq < q_et + n_stage_tasks) iq += kCW;
-        auto load_item = [&](Q2Chunk& dst) {
+        auto load_item = [&](typename FO::Chunk& dst) {
             if (iq >= q_all) return;
             const int row = drow(iq);
             if (ip == 0 && S > 0 && lane * 128 < S * 2) {  // the task's shared down row, into L1
@@ -868,13 +864,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int l = lane; l * 128 < S * 2; l += 32) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
             }
             const int a = ip * L.epp + al;
-            if (a < na) load_q2chunk_global(dbase + (int64_t)row * L.rowF + (int64_t)C.act_e[a] * P.stride, du, dst);
+            if (a < na) FO::load(dbase + (int64_t)row * L.rowF + (int64_t)C.act_e[a] * P.stride, du, dst);
             if (++ip == np) {
                 ip = 0;
                 iq += kCW;
             }
         };
-        Q2Chunk b0{}, b1{}, b2{};
+        typename FO::Chunk b0{}, b1{}, b2{};
         if (ok) {
             load_item(b0);
             load_item(b1);
@@ -923,11 +919,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         wq[q] = (uint32_t)(a0 & 0xffff) | ((uint32_t)a1 << 16);
                         sum += a0 + a1;
                     }
-                    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                    int word, half;
-                    frag_pos(p, word, half);
-                    *reinterpret_cast<uint4*>(row + word) = make_uint4(wq[0], wq[1], wq[2], wq[3]);
-                    if ((p & 15) == 0) row[(word / kFragWords) * kFragWords + 32 + ((p >> 5) & 3)] = (uint32_t)sum;
+                    FO::put8(row, p, wq, sum, true);
                 };
                 auto load8f = [&](int p, float (&hv)[8]) {
                     const float4 a = ld_relaxed_f32x4(hr + p), b = ld_relaxed_f32x4(hr + p + 4);
@@ -991,9 +983,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 1
                     for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
                         const int ent = C.ent_sorted[j];
-                        XFrag f;
-                        load_xfrag_f(hqf + ((size_t)ent * (F / 64) + dc0) * kFragWords, f);
-                        float v = q2k_chunk_dot(b0, du, f);
+                        typename FO::Frag f;
+                        FO::load_frag(hqf + ((size_t)ent * (F / 64) + dc0) * kFragWords, f);
+                        float v = FO::dot(b0, du, f);
                         for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(dgm, v, o);
                         if (dc0 == 0) pb[j] = v * C.hscale[ent];
                     }
@@ -1110,7 +1102,7 @@ static bool plan_fused(const qs_moe_shape& s, int T, int n_sm, size_t smem_max, 
 // Per-device facts the launcher needs on every call, read once per device.
 struct DeviceFacts {
     int n_sm = 0, smem_max = 0;
-    size_t smem_set[4] = {0, 0, 0, 0};  // dynamic smem limit set per kernel instantiation
+    size_t smem_set[8] = {};  // dynamic smem limit set per kernel instantiation
 };
 constexpr int kMaxDevices = 64;
 static DeviceFacts g_dev[kMaxDevices];
@@ -1133,9 +1125,9 @@ static cudaError_t device_facts(DeviceFacts** out) {
     return cudaSuccess;
 }
 
-template <int MAXT, int SLOT>
+template <int MAXT, int FMT, int SLOT>
 static cudaError_t launch_fused_t(const FusedParams& p, size_t smem, DeviceFacts& f, cudaStream_t st) {
-    const void* fn = (const void*)fused_decode_kernel<MAXT>;
+    const void* fn = (const void*)fused_decode_kernel<MAXT, FMT>;
     if (f.smem_set[SLOT] < smem) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -1155,7 +1147,7 @@ static cudaError_t launch_fused_t(const FusedParams& p, size_t smem, DeviceFacts
     at[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, fused_decode_kernel<MAXT>, pp);
+    return cudaLaunchKernelEx(&cfg, fused_decode_kernel<MAXT, FMT>, pp);
 }
 
 bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err) {
@@ -1170,7 +1162,7 @@ bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err) {
 cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
-                                const WsLayout& W, cudaStream_t st, bool x_host_mapped) {
+                                const WsLayout& W, cudaStream_t st, bool x_host_mapped, int fmt) {
     DeviceFacts* f = nullptr;
     cudaError_t e = device_facts(&f);
     if (e != cudaSuccess) return e;
@@ -1214,10 +1206,16 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.off_hq = fp.off_hq;
     p.off_pbuf = fp.off_pbuf;
     p.off_stages = fp.off_stages;
-    if (T == 1) return launch_fused_t<1, 0>(p, fp.smem, *f, st);
-    if (T <= 4) return launch_fused_t<4, 1>(p, fp.smem, *f, st);
-    if (T <= 8) return launch_fused_t<8, 2>(p, fp.smem, *f, st);
-    return launch_fused_t<16, 3>(p, fp.smem, *f, st);
+    if (fmt == kFmtQ4K) {
+        if (T == 1) return launch_fused_t<1, kFmtQ4K, 4>(p, fp.smem, *f, st);
+        if (T <= 4) return launch_fused_t<4, kFmtQ4K, 5>(p, fp.smem, *f, st);
+        if (T <= 8) return launch_fused_t<8, kFmtQ4K, 6>(p, fp.smem, *f, st);
+        return launch_fused_t<16, kFmtQ4K, 7>(p, fp.smem, *f, st);
+    }
+    if (T == 1) return launch_fused_t<1, kFmtQ2K, 0>(p, fp.smem, *f, st);
+    if (T <= 4) return launch_fused_t<4, kFmtQ2K, 1>(p, fp.smem, *f, st);
+    if (T <= 8) return launch_fused_t<8, kFmtQ2K, 2>(p, fp.smem, *f, st);
+    return launch_fused_t<16, kFmtQ2K, 3>(p, fp.smem, *f, st);
 }
 
 }  // namespace qs

@@ -86,7 +86,8 @@ cudaError_t launch_steer_rows(float* y, const float* d, float scale, int T, int 
 cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const float* Wr, const float* bias,
                                 const uint8_t* experts, int64_t stride, const uint16_t* sg, const uint16_t* su,
                                 const uint16_t* sd, const uint16_t* ssig, int T, float* out, void* ws,
-                                const WsLayout& W, cudaStream_t st, bool x_host_mapped = false);
+                                const WsLayout& W, cudaStream_t st, bool x_host_mapped = false,
+                                int fmt = 0 /* 0: Q2_K, 1: Q4_K routed experts */);
 bool fused_decode_supported(const qs_moe_shape& s, int T, cudaError_t* err);
 
 // Decode path of thread-block clusters (qs_cluster.cu): one kernel; a cluster of

@@ -22,7 +22,8 @@ QS_F32, QS_BF16 = 0, 1
 EXPORTS = (
     "qs_status_string", "qs_abi_version", "qs_last_cuda_error", "qs_moe_workspace_bytes", "qs_workspace_init",
     "qs_read_device_status", "qs_route_topk", "qs_group_tokens", "qs_q2k_gemv_grouped", "qs_q2k_down_combine",
-    "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_q2k_quantize", "qs_test_wait_timeout",
+    "qs_shared_expert_ffn", "qs_moe_ffn", "qs_moe_ffn_launches", "qs_moe_ffn_q4k_launches", "qs_q2k_quantize",
+    "qs_test_wait_timeout",
     "qs_moe_ffn_noalloc", "qs_steer_rows", "qs_moe_ffn_q4k", "qs_q4k_quantize", "qs_moe_host_workspace_bytes",
     "qs_moe_ffn_host", "qs_noalloc_read_device_status", "qs_read_routing", "qs_moe_ffn_cluster",
 )
@@ -89,6 +90,7 @@ def load(build_if_missing: bool = True):
     L.qs_moe_ffn.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
     L.qs_moe_ffn_cluster.argtypes = [SP, P, P, P, EP, HP, P, i32, P, sz, P]
     L.qs_moe_ffn_launches.argtypes = [SP, i32, i32]
+    L.qs_moe_ffn_q4k_launches.argtypes = [SP, i32, i32]
     L.qs_moe_ffn_noalloc.argtypes = [SP, P, P, P, EP, HP, P, i32, P]
     L.qs_noalloc_read_device_status.restype = i32
     L.qs_read_routing.argtypes = [SP, i32, P, sz, P, P, P]
@@ -304,6 +306,10 @@ def alloc_host_workspace(shape: qs_moe_shape, max_tokens: int, device="cuda"):
 
 def qs_moe_ffn_launches(shape, n_tokens, has_shared=True) -> int:
     return load().qs_moe_ffn_launches(ctypes.byref(shape), n_tokens, int(bool(has_shared)))
+
+
+def qs_moe_ffn_q4k_launches(shape, n_tokens, has_shared=True) -> int:
+    return load().qs_moe_ffn_q4k_launches(ctypes.byref(shape), n_tokens, int(bool(has_shared)))
 
 
 def qs_q2k_quantize(w, out, stream=None):

@@ -248,10 +248,14 @@ int qs_noalloc_read_device_status(void *stream);
 /* The whole layer with Q4_K routed experts: the same routing, grouping and
  * gated bf16 shared expert as qs_moe_ffn, the routed gate/up (SwiGLU) and down
  * projections dequantising Q4_K blocks (w = d*sc*q - dmin*m per 32-weight
- * sub-block) against fp32 activations with fp32 accumulation.  Arguments,
- * layouts, workspace (qs_moe_workspace_bytes of the same shape) and error
- * behaviour as qs_moe_ffn; expert_stride must cover 144*3*F*H/256 bytes.
- * Runs the per-step kernels: up to six launches on `stream`. */
+ * sub-block).  Arguments, layouts, workspace (qs_moe_workspace_bytes of the
+ * same shape) and error behaviour as qs_moe_ffn; expert_stride must cover
+ * 144*3*F*H/256 bytes and be a multiple of 16.  Where the persistent decode
+ * kernel plans the call (the token counts it takes for qs_moe_ffn) it is one
+ * launch: activations quantised per token to int16 with a max-abs scale,
+ * per-chunk integer sums exact, d and dmin applied in fp32.  Otherwise the
+ * per-step kernels (fp32 activations, fp32 accumulation): up to six launches
+ * on `stream`. */
 int qs_moe_ffn_q4k(const qs_moe_shape *shape, const void *x, const float *router_w, const float *router_bias,
                    const qs_q4k_experts *experts, const qs_shared_expert *shared, float *out, int n_tokens,
                    void *workspace, size_t workspace_bytes, void *stream);
@@ -313,6 +317,11 @@ int qs_read_routing(const qs_moe_shape *shape, int n_tokens, const void *workspa
  * memset), 4 or 5 for the per-step path; 0 on an invalid shape, negative
  * (-cudaError_t) if the device query fails. */
 int qs_moe_ffn_launches(const qs_moe_shape *shape, int n_tokens, int has_shared);
+
+/* The same count for qs_moe_ffn_q4k: 1 for the persistent decode kernel, else
+ * 6 (4 without the shared expert); 0 on an invalid shape, negative
+ * (-cudaError_t) if the device query fails. */
+int qs_moe_ffn_q4k_launches(const qs_moe_shape *shape, int n_tokens, int has_shared);
 
 /* Q2_K encoder (weight set-up, not part of the layer): round-to-nearest,
  * per sub-block m = max(0, -min), s = (max + m)/3, per block d = fp16(max s

@@ -128,3 +128,34 @@ def test_run_to_run_bitwise():
     a = L.run_gpu()
     b = L.run_gpu()
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("T,launches", [(1, 1), (4, 1), (20, 6)])
+def test_layer_paths(T, launches):
+    """The persistent decode kernel takes the call where it plans it (one launch), the per-step
+    kernels the rest; both against the oracle."""
+    shape = qi.LayerShape(1024, 64, 8, 512, 512, qi.BF16)
+    s = qm.make_shape(shape.hidden, shape.n_experts, shape.top_k, shape.expert_ffn, shape.shared_ffn, shape.x_dtype)
+    assert qm.qs_moe_ffn_q4k_launches(s, T, True) == launches
+    L = Q4Layer(shape, seed=90 + T, T=T)
+    got = L.run_gpu()
+    ref = L.run_oracle()
+    keep = ref["margin"] >= MARGIN
+    assert keep.any()
+    assert_close(got[keep], ref["y"][keep], what=f"Q4_K layer, {T} tokens, {launches} launch(es)")
+
+
+def test_one_kernel_batch_equals_single_calls():
+    """One call of 4 tokens on the persistent kernel gives each token the bits of its own call."""
+    shape = qi.LayerShape(2048, 32, 8, 512, 512, qi.BF16)
+    L = Q4Layer(shape, seed=55, T=4)
+    s = qm.make_shape(shape.hidden, shape.n_experts, shape.top_k, shape.expert_ffn, shape.shared_ffn, shape.x_dtype)
+    assert qm.qs_moe_ffn_q4k_launches(s, 4, True) == 1 and qm.qs_moe_ffn_q4k_launches(s, 1, True) == 1
+    batch = L.run_gpu()
+    xb = L.xb
+    singles = []
+    for t in range(4):
+        L.xb, L.T = xb[t:t + 1], 1
+        singles.append(L.run_gpu())
+    L.xb, L.T = xb, 4
+    assert np.array_equal(batch, np.concatenate(singles))
