@@ -719,12 +719,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int nch = L.cpr / cstep;
         const unsigned gm = L.cpr >= 32 ? 0xffffffffu : (((1u << L.cpr) - 1u) << (lane & ~(L.cpr - 1)));
         const int g0 = first_owned(L.n_ind, L.G, L.cta);
-        // first byte of this lane's gate row of task qq (the up row is F rows further)
-        auto task_row = [&](int qq) -> const uint8_t* {
-            const int m = qq / L.ept, rt = qq % L.ept;
+        // A task's position: tile m of this CTA, task rt inside it, active expert a and its tile
+        // tt.  Found by division once, then advanced by kCW tasks with a few subtractions.
+        struct TaskPos {
+            int rt, a, tt;
+        };
+        auto task_pos = [&](int qq) {
+            TaskPos t;
+            const int m = qq / L.ept;
+            t.rt = qq - m * L.ept;
             const int idx = g0 + m * L.G - L.n_ind;
-            const int a = idx / L.tpe, tt = idx % L.tpe;
-            return P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw + rl) * L.rowH;
+            t.a = idx / L.tpe;
+            t.tt = idx - t.a * L.tpe;
+            return t;
+        };
+        auto task_next = [&](TaskPos& t) {
+            t.rt += kCW;
+            while (t.rt >= L.ept) {  // next tile of this CTA: G tiles further
+                t.rt -= L.ept;
+                t.tt += L.G;
+            }
+            while (t.tt >= L.tpe) {
+                t.tt -= L.tpe;
+                t.a++;
+            }
+        };
+        // first byte of this lane's gate row of a task (the up row is F rows further)
+        auto task_row = [&](const TaskPos& t) -> const uint8_t* {
+            return P.experts + (int64_t)C.act_e[t.a] * P.stride + (int64_t)(t.tt * P.R + t.rt * L.rpw + rl) * L.rowH;
         };
         const int64_t up_off = (int64_t)P.F * L.rowH;
         // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
@@ -733,7 +755,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         typename FO::Chunk pg, pu;  // the next item's words, in flight
         if (ok && q < q_et) {  // the first task's rows, requested before the L2 requests below
             if (hoist) FO::load_frag(xqf + (size_t)c0 * kFragWords, fx);
-            const uint8_t* gr = task_row(q);
+            const uint8_t* gr = task_row(task_pos(q));
             FO::load(gr + (c0 >> 2) * FO::kBlock, c0 & 3, pg);
             FO::load(gr + up_off + (c0 >> 2) * FO::kBlock, c0 & 3, pu);
         }
@@ -770,12 +792,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             }
         }
         if (ok && q < q_et) {
+            TaskPos cur = task_pos(q), nxt = cur;
+            task_next(nxt);
 #pragma unroll 1
             for (; q < q_et; q += kCW) {
-                const int m = q / L.ept, rt = q % L.ept;
-                const int idx = g0 + m * L.G - L.n_ind;
-                const int a = idx / L.tpe, tt = idx % L.tpe;
-                const int r = rt * L.rpw + rl;
+                const int a = cur.a, tt = cur.tt;
+                const int r = cur.rt * L.rpw + rl;
+                const uint8_t* grow = task_row(cur);
                 const int j0 = C.act_begin[a], ne = C.act_begin[a + 1] - j0;
                 float gacc[MAXT], uacc[MAXT];
 #pragma unroll
@@ -786,11 +809,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     const typename FO::Chunk gc = pg, uc = pu;
                     // request the next item: this task's next chunk, or the next task's first
                     if (i + 1 < nch) {
-                        const uint8_t* gr = task_row(q) + ((c + cstep) >> 2) * FO::kBlock;
+                        const uint8_t* gr = grow + ((c + cstep) >> 2) * FO::kBlock;
                         FO::load(gr, (c + cstep) & 3, pg);
                         FO::load(gr + up_off, (c + cstep) & 3, pu);
                     } else if (q + kCW < q_et) {
-                        const uint8_t* gr = task_row(q + kCW) + (c0 >> 2) * FO::kBlock;
+                        const uint8_t* gr = task_row(nxt) + (c0 >> 2) * FO::kBlock;
                         FO::load(gr, c0 & 3, pg);
                         FO::load(gr + up_off, c0 & 3, pu);
                     }
@@ -836,6 +859,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         publish(C, ctr_h, kPubH);
                     }
                 }
+                cur = nxt;
+                task_next(nxt);
             }
         }
         // ---------------------------------------------------------- down rows: setup
@@ -856,9 +881,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         };
         int iq = q, ip = 0;  // next item to request
         while (iq < q_et + n_stage_tasks) iq += kCW;
+        int irow = iq < q_all ? drow(iq) : 0;  // its task's output row
         auto load_item = [&](typename FO::Chunk& dst) {
             if (iq >= q_all) return;
-            const int row = drow(iq);
+            const int row = irow;
             if (ip == 0 && S > 0 && lane * 128 < S * 2) {  // the task's shared down row, into L1
                 const uint16_t* srow = P.sd + (size_t)row * S;
                 for (int l = lane; l * 128 < S * 2; l += 32) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
@@ -868,6 +894,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             if (++ip == np) {
                 ip = 0;
                 iq += kCW;
+                if (iq < q_all) irow = drow(iq);
             }
         };
         typename FO::Chunk b0{}, b1{}, b2{};
