@@ -194,6 +194,27 @@ __device__ __forceinline__ int owned_count(int lo, int hi, int G, int cta) {
     return f < hi ? (hi - 1 - f) / G + 1 : 0;
 }
 
+// n / d and n % d for 0 <= n < 2^24 through a float reciprocal and one correction step
+// (cheaper than an integer division by a value known only at run time).
+struct FDiv {
+    float inv;
+    int d;
+};
+__device__ __forceinline__ FDiv fdiv_of(int d) { return FDiv{1.0f / (float)d, d}; }
+__device__ __forceinline__ int fdiv(int n, const FDiv& f, int& rem) {
+    int q = __float2int_rz(__int2float_rn(n) * f.inv);
+    int r = n - q * f.d;
+    if (r < 0) {
+        q--;
+        r += f.d;
+    } else if (r >= f.d) {
+        q++;
+        r -= f.d;
+    }
+    rem = r;
+    return q;
+}
+
 __device__ __forceinline__ Plan make_plan(const FusedParams& P, int block_bytes) {
     Plan L;
     L.G = gridDim.x;
@@ -768,20 +789,25 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             const int lines_d = (P.RD * L.rowF + 127) / 128 + 1;  // + 1: the rows need not start on a line
             const int n_d = own_dg * na * lines_d;
             const int f_et = first_owned(L.n_ind, L.G, L.cta), f_dg = first_owned(lo_dg, L.G, L.cta);
+            const FDiv d_l2 = fdiv_of(2 * lines_gu), d_ept = fdiv_of(L.ept), d_tpe = fdiv_of(L.tpe),
+                       d_ld = fdiv_of(lines_d), d_na = fdiv_of(na > 0 ? na : 1);
 #pragma unroll 1
             for (int i = tid; ok && i < n_gu + n_d; i += kCT) {
                 const uint8_t* p;
                 if (i < n_gu) {
-                    const int q = i / (2 * lines_gu), l = i % (2 * lines_gu);
-                    const int m = q / L.ept, rt = q % L.ept;
+                    int l, rt, tt;
+                    const int q = fdiv(i, d_l2, l);
+                    const int m = fdiv(q, d_ept, rt);
                     const int idx = f_et + m * L.G - L.n_ind;
-                    const int a = idx / L.tpe, tt = idx % L.tpe;
+                    const int a = fdiv(idx, d_tpe, tt);
+                    const bool up = l >= lines_gu;
                     p = P.experts + (int64_t)C.act_e[a] * P.stride + (int64_t)(tt * P.R + rt * L.rpw) * L.rowH +
-                        (l >= lines_gu ? (int64_t)P.F * L.rowH : 0) + (int64_t)(l % lines_gu) * 128;
+                        (up ? (int64_t)P.F * L.rowH : 0) + (int64_t)(up ? l - lines_gu : l) * 128;
                 } else {
                     const int j = i - n_gu;
-                    const int q = j / lines_d, l = j % lines_d;
-                    const int m = q / na, a = q % na;
+                    int l, a;
+                    const int q = fdiv(j, d_ld, l);
+                    const int m = fdiv(q, d_na, a);
                     const int r0 = (f_dg + m * L.G - lo_dg) * P.RD;
                     const uint8_t* row0 = P.experts + (int64_t)C.act_e[a] * P.stride + down_off + (int64_t)r0 * L.rowF;
                     const uint8_t* lim = row0 + (int64_t)P.RD * L.rowF;

@@ -660,7 +660,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
             mbar_init(&ctl->aempty[s], 1);
         }
         for (int s = 0; s < NW; s++) {
-            mbar_init(&ctl->wfull[s], kDeqWarps);
+            mbar_init(&ctl->wfull[s], kDeqWarps / 2);
             mbar_init(&ctl->wempty[s], 1);
         }
         for (int r = 0; r < NRV; r++) {
@@ -710,9 +710,10 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
 
     if (warp < kDeqWarps) {
         // ---------------------------------------------------------- dequant warps: raw slot -> W stage
-        // Thread: weight row r of the unit (gate/up: rows 0..127 gate, 128..255 up), K half jj of
-        // every slice.  A stage is full once all sixteen warps have stored their rows.
-        const int r = 32 * (warp & 7) + lane, jj = warp >> 3;
+        // Thread: weight row r of the unit (gate/up: rows 0..127 gate, 128..255 up), both K halves
+        // of the slices of its group's parity (warps 0..7 even slices, 8..15 odd).  A stage is full
+        // once the eight warps of its group have stored their rows.
+        const int r = 32 * (warp & 7) + lane, grp = warp >> 3;
         int GW = 0, C = 0;
         for_units(p, tb, n_groups, [&](const Unit& U) -> bool {
             if (warp_aborted(abort)) return false;
@@ -727,9 +728,11 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                 int s, fill;
                 w_stage(g, NW, s, fill);
                 uint32_t v[16];
-                dequant_half(scw, qw, c, jj, d, dm, v);
+                dequant_half(scw, qw, c, 0, d, dm, v);
                 if (fill > 0 && !lead_wait(&ctl->wempty[s], (fill - 1) & 1, abort, p.status, 3, g)) return false;
-                store_w_half(wst + s * kWBytes, r, jj, v);
+                store_w_half(wst + s * kWBytes, r, 0, v);
+                dequant_half(scw, qw, c, 1, d, dm, v);
+                store_w_half(wst + s * kWBytes, r, 1, v);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic stores -> MMA reads
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctl->wfull[s]);
@@ -768,8 +771,8 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         q0[i] = w[4 + i];
                         q1[i] = w[12 + i];
                     }
-                    if (!slice(4 * ch + 0, 0, w[0], q0, d, dm) || !slice(4 * ch + 1, 1, w[1], q0, d, dm) ||
-                        !slice(4 * ch + 2, 2, w[2], q1, d, dm) || !slice(4 * ch + 3, 3, w[3], q1, d, dm))
+                    if (!slice(4 * ch + grp, grp, grp ? w[1] : w[0], q0, d, dm) ||
+                        !slice(4 * ch + 2 + grp, 2 + grp, grp ? w[3] : w[2], q1, d, dm))
                         return false;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->rawfree[slot]);
@@ -782,7 +785,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                     return false;
                 const uint32_t row = smem_u32(raw + slot * SLOT) + (uint32_t)(r & 127) * p.rowbytes;
 #pragma unroll 1
-                for (int kb = 0; kb < KB; kb++) {
+                for (int kb = grp; kb < KB; kb += 2) {
                     const uint32_t blk = row + 84u * (uint32_t)(kb >> 2);
                     const int c = kb & 3;
                     uint32_t qw[8];
@@ -968,7 +971,7 @@ __global__ void __launch_bounds__(kExpertThreads, 1) pf_expert_kernel(const __gr
                         uint64_t* bar = &ctl->wfull[s];
                         wt_last[s] = g;
                         mbar_arrive_expect_tx(bar, kWBytes);
-                        mbar_arrive_count(bar, kDeqWarps - 1);
+                        mbar_arrive_count(bar, kDeqWarps / 2 - 1);
                         if (NM == 2) {
                             tma_load_2d(w, &p.map_s0, kb * 64, U.mt * 128, bar);
                             tma_load_2d(w + kWBytes / 2, &p.map_s1, kb * 64, U.mt * 128, bar);
