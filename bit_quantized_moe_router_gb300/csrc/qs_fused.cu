@@ -1028,6 +1028,47 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 1
         for (; ok && q < q_all; q += kCW) {
             const int row = drow(q);
+            if (MAXT == 1) {
+                // one token: one entry per active expert; two passes at a time, their two dot
+                // chains independent (the same sums, the same order)
+#pragma unroll 1
+                for (int pa = 0; pa < np; pa += 2) {
+                    const bool two = pa + 1 < np;  // the stream holds passes pa, pa + 1 in b0, b1
+                    typename FO::Chunk b3{};
+                    load_item(b2);
+                    if (two) load_item(b3);
+                    const int a0 = pa * L.epp + al, a1 = a0 + L.epp;
+                    const bool h0 = a0 < na, h1 = two && a1 < na;
+                    const int j0 = h0 ? C.act_begin[a0] : 0, j1 = h1 ? C.act_begin[a1] : 0;
+                    const int e0 = C.ent_sorted[j0], e1 = C.ent_sorted[j1];
+                    float v0 = 0.0f, v1 = 0.0f;
+                    if (h0) {
+                        typename FO::Frag f0;
+                        FO::load_frag(hqf + ((size_t)e0 * (F / 64) + dc0) * kFragWords, f0);
+                        v0 = FO::dot(b0, du, f0);
+                    }
+                    if (h1) {
+                        typename FO::Frag f1;
+                        FO::load_frag(hqf + ((size_t)e1 * (F / 64) + dc0) * kFragWords, f1);
+                        v1 = FO::dot(b1, du, f1);
+                    }
+                    for (int o = L.cpf >> 1; o > 0; o >>= 1) {
+                        v0 += __shfl_xor_sync(dgm, v0, o);
+                        v1 += __shfl_xor_sync(dgm, v1, o);
+                    }
+                    if (dc0 == 0) {
+                        if (h0) pb[j0] = v0 * C.hscale[e0];
+                        if (h1) pb[j1] = v1 * C.hscale[e1];
+                    }
+                    if (two) {
+                        b0 = b2;
+                        b1 = b3;
+                    } else {  // b1 already holds the next task's first item
+                        b0 = b1;
+                        b1 = b2;
+                    }
+                }
+            } else {
 #pragma unroll 1
             for (int pa = 0; pa < np; pa++) {
                 load_item(b2);
@@ -1045,6 +1086,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 }
                 b0 = b1;
                 b1 = b2;
+            }
             }
             // shared expert down row
             float sacc[MAXT];
