@@ -820,6 +820,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         if (ok && q < q_et) {
             TaskPos cur = task_pos(q), nxt = cur;
             task_next(nxt);
+            int n_done = 0;
 #pragma unroll 1
             for (; q < q_et; q += kCW) {
                 const int a = cur.a, tt = cur.tt;
@@ -876,17 +877,20 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         }
                     }
                 }
-                __syncwarp();  // orders the lanes' h stores before lane 0's fences below
-                // the CTA's last routed task publishes all of the CTA's h tiles
-                if (lane == 0) {
-                    __threadfence_block();
-                    if (atomicSub(&C.et_left, 1) == 1) {
-                        __threadfence_block();
-                        publish(C, ctr_h, kPubH);
-                    }
-                }
+                n_done++;
                 cur = nxt;
                 task_next(nxt);
+            }
+            // the warp whose tasks complete the CTA's count publishes all of the CTA's h tiles.  Once
+            // per warp, after its last task: a fence waits for the warp's loads in flight too, and
+            // one per task would stall every next task's rows
+            __syncwarp();  // orders the lanes' h stores before lane 0's fences below
+            if (lane == 0) {
+                __threadfence_block();
+                if (atomicSub(&C.et_left, n_done) == n_done) {
+                    __threadfence_block();
+                    publish(C, ctr_h, kPubH);
+                }
             }
         }
         // ---------------------------------------------------------- down rows: setup
