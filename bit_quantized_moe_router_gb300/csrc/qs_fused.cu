@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll
                         for (int e = 0; e < MAXT; e++) {
                             if (e < ne) {
-                                const int t = C.ent_sorted[j0 + e] / k;
+                                const int t = C.es_tok[j0 + e];
                                 float dg, du;
                                 FO::dot2(gc, uc, c & 3, xqf + ((size_t)t * (H / 64) + c) * kFragWords, dg, du);
                                 gacc[e] += dg;
@@ -866,13 +866,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int e = 0; e < MAXT; e++) {
                     if (e < ne) {
                         float gv = gacc[e], uv = uacc[e];
-                        for (int o = min(L.cpr, 32) >> 1; o > 0; o >>= 1) {
-                            gv += __shfl_xor_sync(gm, gv, o);
-                            uv += __shfl_xor_sync(gm, uv, o);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+                            if (o < L.cpr) {
+                                gv += __shfl_xor_sync(gm, gv, o);
+                                uv += __shfl_xor_sync(gm, uv, o);
+                            }
                         }
                         if (c0 == 0) {
                             const int ent = C.ent_sorted[j0 + e];
-                            const float sx = C.xscale[ent / k] * (1.0f / 32767.0f);
+                            const float sx = C.xscale[C.es_tok[j0 + e]] * (1.0f / 32767.0f);
                             P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
                         }
                     }
@@ -1056,9 +1059,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         FO::load_frag(hqf + ((size_t)e1 * (F / 64) + dc0) * kFragWords, f1);
                         v1 = FO::dot(b1, du, f1);
                     }
-                    for (int o = L.cpf >> 1; o > 0; o >>= 1) {
-                        v0 += __shfl_xor_sync(dgm, v0, o);
-                        v1 += __shfl_xor_sync(dgm, v1, o);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        if (o < L.cpf) {
+                            v0 += __shfl_xor_sync(dgm, v0, o);
+                            v1 += __shfl_xor_sync(dgm, v1, o);
+                        }
                     }
                     if (dc0 == 0) {
                         if (h0) pb[j0] = v0 * C.hscale[e0];
@@ -1084,7 +1090,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         typename FO::Frag f;
                         FO::load_frag(hqf + ((size_t)ent * (F / 64) + dc0) * kFragWords, f);
                         float v = FO::dot(b0, du, f);
-                        for (int o = L.cpf >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(dgm, v, o);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1)
+                            if (o < L.cpf) v += __shfl_xor_sync(dgm, v, o);
                         if (dc0 == 0) pb[j] = v * C.hscale[ent];
                     }
                 }
