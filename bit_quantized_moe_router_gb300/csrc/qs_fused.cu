@@ -88,7 +88,7 @@ struct FusedParams {
     float* out;
     float* xlog;  // [T x E] logits
     float* xhs;   // [T x S] hs
-    float* xh;    // [T*k x F] h
+    float* xh;    // [T*k x F] h, rows in sorted entry order
     WsHeader* hdr;
     int32_t* rec_ids;  // [T*k] the call's routing (written by CTA 0)
     float* rec_p;      // [T*k]
@@ -130,7 +130,8 @@ struct alignas(16) FusedCtl {
     int wcnt[8];
     float gate_s[kMaxT];
     float xscale[kMaxT];
-    float hscale[kMaxEnt];
+    float hscale[kMaxEnt];       // scale of the int16 h row of ent_sorted[i]
+    float ps[kMaxEnt];           // routing weight of ent_sorted[i]
     float red[2 * kGTB];
 };
 
@@ -520,6 +521,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         }
                         if (act) {
                             C.ent_sorted[rank] = lane;
+                            C.ps[rank] = C.p[lane];
                             C.es[rank] = e;
                             C.es_tok[rank] = lane / k;
                         }
@@ -565,6 +567,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                             rank += (f < e) | ((f == e) & (j < i));
                         }
                         C.ent_sorted[rank] = i;
+                        C.ps[rank] = C.p[i];
                         C.es[rank] = e;
                         C.es_tok[rank] = i / k;
                     }
@@ -874,9 +877,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                             }
                         }
                         if (c0 == 0) {
-                            const int ent = C.ent_sorted[j0 + e];
                             const float sx = C.xscale[C.es_tok[j0 + e]] * (1.0f / 32767.0f);
-                            P.xh[(size_t)ent * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
+                            P.xh[(size_t)(j0 + e) * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
                         }
                     }
                 }
@@ -908,9 +910,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int f_dg = first_owned(lo_dg, L.G, L.cta);
         float* pb = pbuf + warp * kMaxEnt;
         const uint8_t* dbase = P.experts + 2ll * P.F * L.rowH + (dc0 >> 2) * FO::kBlock;
+        const int rd_sh = __ffs(P.RD) - 1;  // RD is a power of two
         auto drow = [&](int qq) -> int {  // output row of down task qq
             const int dq = qq - q_et - n_stage_tasks;
-            return (f_dg + (dq / P.RD) * L.G - lo_dg) * P.RD + dq % P.RD;
+            return (f_dg + (dq >> rd_sh) * L.G - lo_dg) * P.RD + (dq & (P.RD - 1));
         };
         int iq = q, ip = 0;  // next item to request
         while (iq < q_et + n_stage_tasks) iq += kCW;
@@ -957,7 +960,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&C.hs_bar);
             } else {
-                const int ent = sidx - (S > 0 ? 1 : 0);
+                const int ent = sidx - (S > 0 ? 1 : 0);  // sorted position
                 // the first entry task to get here waits for the h counter; the others for its flag
                 int got = 1;
                 if (lane == 0 && atomicCAS(&C.h_poller, 0, 1) == 0) {
@@ -1047,16 +1050,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     const int a0 = pa * L.epp + al, a1 = a0 + L.epp;
                     const bool h0 = a0 < na, h1 = two && a1 < na;
                     const int j0 = h0 ? C.act_begin[a0] : 0, j1 = h1 ? C.act_begin[a1] : 0;
-                    const int e0 = C.ent_sorted[j0], e1 = C.ent_sorted[j1];
                     float v0 = 0.0f, v1 = 0.0f;
                     if (h0) {
                         typename FO::Frag f0;
-                        FO::load_frag(hqf + ((size_t)e0 * (F / 64) + dc0) * kFragWords, f0);
+                        FO::load_frag(hqf + ((size_t)j0 * (F / 64) + dc0) * kFragWords, f0);
                         v0 = FO::dot(b0, du, f0);
                     }
                     if (h1) {
                         typename FO::Frag f1;
-                        FO::load_frag(hqf + ((size_t)e1 * (F / 64) + dc0) * kFragWords, f1);
+                        FO::load_frag(hqf + ((size_t)j1 * (F / 64) + dc0) * kFragWords, f1);
                         v1 = FO::dot(b1, du, f1);
                     }
 #pragma unroll
@@ -1067,8 +1069,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         }
                     }
                     if (dc0 == 0) {
-                        if (h0) pb[j0] = v0 * C.hscale[e0];
-                        if (h1) pb[j1] = v1 * C.hscale[e1];
+                        if (h0) pb[j0] = v0 * C.hscale[j0];
+                        if (h1) pb[j1] = v1 * C.hscale[j1];
                     }
                     if (two) {
                         b0 = b2;
@@ -1086,14 +1088,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 if (a < na) {
 #pragma unroll 1
                     for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                        const int ent = C.ent_sorted[j];
                         typename FO::Frag f;
-                        FO::load_frag(hqf + ((size_t)ent * (F / 64) + dc0) * kFragWords, f);
+                        FO::load_frag(hqf + ((size_t)j * (F / 64) + dc0) * kFragWords, f);
                         float v = FO::dot(b0, du, f);
 #pragma unroll
                         for (int o = 16; o > 0; o >>= 1)
                             if (o < L.cpf) v += __shfl_xor_sync(dgm, v, o);
-                        if (dc0 == 0) pb[j] = v * C.hscale[ent];
+                        if (dc0 == 0) pb[j] = v * C.hscale[j];
                     }
                 }
                 b0 = b1;
@@ -1110,10 +1111,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             for (int t = 0; t < MAXT; t++) {
                 if (t < T && lane == t) {
                     float acc = 0.0f;
+                    if (MAXT == 1) {  // one token: its entries are sorted positions 0 .. k-1
+#pragma unroll 8
+                        for (int j = 0; j < k; j++) acc = fmaf(C.ps[j], pb[j], acc);
+                    } else {
 #pragma unroll 1
-                    for (int mm = 0; mm < k; mm++) {
-                        const int j = C.tok_sorted[t * k + mm];
-                        acc = fmaf(C.p[C.ent_sorted[j]], pb[j], acc);
+                        for (int mm = 0; mm < k; mm++) {
+                            const int j = C.tok_sorted[t * k + mm];
+                            acc = fmaf(C.ps[j], pb[j], acc);
+                        }
                     }
                     if (S > 0) acc = fmaf(C.gate_s[t], sacc[t], acc);
                     P.out[(size_t)t * H + row] = acc;
