@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     }
                 }
                 group_sync<kGTA>(2);
-                if (n_ent <= 32) {
+                if (MAXT == 1 || n_ent <= 32) {  // (the one-token kernel runs only with k <= 32)
                     // one warp: entries ordered by (expert, entry) with shuffles, then the active
                     // experts and each token's entries, without further group barriers
                     if (gwarp == 0) {
@@ -693,7 +693,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const int j = first_owned(L.n_rt, L.G, L.cta) + m * L.G - L.n_rt;
                 const size_t row = (size_t)j * P.RS + r;
                 const uint8_t *gw, *uw;
-                if (P.sg_direct) {  // from global memory (prefetched into L2 before the previous grid ended)
+                if (MAXT == 1 || P.sg_direct) {  // from global memory (prefetched into L2 before the previous
+                                                 // grid ended; always for one token)
                     gw = reinterpret_cast<const uint8_t*>(P.sg + row * H);
                     uw = reinterpret_cast<const uint8_t*>(P.su + row * H);
                 } else {
@@ -708,7 +709,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll
                 for (int t = 0; t < MAXT; t++)
                     if (t < T && lane == t) P.xhs[(size_t)t * S + row] = silu(ga[t]) * ua[t];
-                if (!P.sg_direct) release_slot(C, sq % ns, P.RS);
+                if (!(MAXT == 1 || P.sg_direct)) release_slot(C, sq % ns, P.RS);
             }
             if (!ok) fail(C, status);
             // every hs row of this CTA is stored: publish them (the barrier orders the stores)
@@ -1320,12 +1321,12 @@ cudaError_t launch_fused_decode(const qs_moe_shape& s, const void* x, const floa
     p.off_pbuf = fp.off_pbuf;
     p.off_stages = fp.off_stages;
     if (fmt == kFmtQ4K) {
-        if (T == 1) return launch_fused_t<1, kFmtQ4K, 4>(p, fp.smem, *f, st);
+        if (T == 1 && s.top_k <= 32) return launch_fused_t<1, kFmtQ4K, 4>(p, fp.smem, *f, st);
         if (T <= 4) return launch_fused_t<4, kFmtQ4K, 5>(p, fp.smem, *f, st);
         if (T <= 8) return launch_fused_t<8, kFmtQ4K, 6>(p, fp.smem, *f, st);
         return launch_fused_t<16, kFmtQ4K, 7>(p, fp.smem, *f, st);
     }
-    if (T == 1) return launch_fused_t<1, kFmtQ2K, 0>(p, fp.smem, *f, st);
+    if (T == 1 && s.top_k <= 32) return launch_fused_t<1, kFmtQ2K, 0>(p, fp.smem, *f, st);
     if (T <= 4) return launch_fused_t<4, kFmtQ2K, 1>(p, fp.smem, *f, st);
     if (T <= 8) return launch_fused_t<8, kFmtQ2K, 2>(p, fp.smem, *f, st);
     return launch_fused_t<16, kFmtQ2K, 3>(p, fp.smem, *f, st);

@@ -211,8 +211,9 @@ __device__ __forceinline__ void warp_topk(const float* l, int E, int k, int& id,
 }
 
 // The same selection for E <= 1024 with few registers: every round re-reads the logits
-// (L1/L2 hits after the first) instead of holding them.
-__device__ __forceinline__ void warp_topk_stream(const float* l, int E, int k, int& id, float& w) {
+// (L1/L2 hits after the first) instead of holding them.  Out of line: kept apart from the code of
+// the common case.
+static __device__ __noinline__ void warp_topk_stream(const float* l, int E, int k, int& id, float& w) {
     const int lane = threadIdx.x & 31;
     const int nm = (E + 31) >> 5;
     uint32_t taken = 0, my_key = 0;
