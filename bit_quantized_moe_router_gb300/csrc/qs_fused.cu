@@ -125,6 +125,7 @@ struct alignas(16) FusedCtl {
     int es[kMaxEnt];             // expert of ent_sorted[i]
     int es_tok[kMaxEnt];         // token of ent_sorted[i]
     int act_e[kMaxEnt];          // active experts, ascending
+    const uint8_t* act_w[kMaxEnt];  // first byte of each active expert's weights
     int act_begin[kMaxEnt + 1];  // first ent_sorted index of each active expert
     int tok_sorted[kMaxEnt];     // per token, its k ent_sorted indices, ascending
     int wcnt[8];
@@ -534,6 +535,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         const int ai = __popc(bal & ((2u << lane) - 1u)) - 1;
                         if (start) {
                             C.act_e[ai] = er;
+                            C.act_w[ai] = P.experts + (int64_t)er * P.stride;
                             C.act_begin[ai] = lane;
                         }
                         if (lane == n_ent - 1) {
@@ -583,6 +585,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                         for (int w = 0; w < gwarp; w++) a += C.wcnt[w];
                         if (start) {
                             C.act_e[a] = C.es[gtid];
+                            C.act_w[a] = P.experts + (int64_t)C.es[gtid] * P.stride;
                             C.act_begin[a] = gtid;
                         }
                         if (gtid == n_ent - 1) {
@@ -771,7 +774,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         };
         // first byte of this lane's gate row of a task (the up row is F rows further)
         auto task_row = [&](const TaskPos& t) -> const uint8_t* {
-            return P.experts + (int64_t)C.act_e[t.a] * P.stride + (int64_t)(t.tt * P.R + t.rt * L.rpw + rl) * L.rowH;
+            return C.act_w[t.a] + (int64_t)(t.tt * P.R + t.rt * L.rpw + rl) * L.rowH;
         };
         const int64_t up_off = (int64_t)P.F * L.rowH;
         // one token and one chunk per lane: that chunk of the token's int16 x, once for every task
@@ -910,7 +913,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
         const int np = (na + L.epp - 1) / L.epp;
         const int f_dg = first_owned(lo_dg, L.G, L.cta);
         float* pb = pbuf + warp * kMaxEnt;
-        const uint8_t* dbase = P.experts + 2ll * P.F * L.rowH + (dc0 >> 2) * FO::kBlock;
+        const int64_t dbase = 2ll * P.F * L.rowH + (dc0 >> 2) * FO::kBlock;  // this lane's bytes of a down row
         const int rd_sh = __ffs(P.RD) - 1;  // RD is a power of two
         auto drow = [&](int qq) -> int {  // output row of down task qq
             const int dq = qq - q_et - n_stage_tasks;
@@ -927,17 +930,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 for (int l = lane; l * 128 < S * 2; l += 32) asm volatile("prefetch.global.L1 [%0];" ::"l"(srow + l * 64));
             }
             const int a = ip * L.epp + al;
-            if (a < na) FO::load(dbase + (int64_t)row * L.rowF + (int64_t)C.act_e[a] * P.stride, du, dst);
+            if (a < na) FO::load(C.act_w[a] + dbase + (int64_t)row * L.rowF, du, dst);
             if (++ip == np) {
                 ip = 0;
                 iq += kCW;
                 if (iq < q_all) irow = drow(iq);
             }
         };
-        typename FO::Chunk b0{}, b1{}, b2{};
+        typename FO::Chunk b0{}, b1{}, b2{}, b3{};
         if (ok) {
             load_item(b0);
             load_item(b1);
+            if (MAXT == 1) {  // one token: the stream runs two pass pairs ahead
+                load_item(b2);
+                load_item(b3);
+            }
         }
         // ---------------------------------------------------------- staging of hs / of one entry's int16 h
 #pragma unroll 1
@@ -1045,12 +1052,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll 1
                 for (int pa = 0; pa < np; pa += 2) {
                     const bool two = pa + 1 < np;  // the stream holds passes pa, pa + 1 in b0, b1
-                    typename FO::Chunk b3{};
-                    load_item(b2);
-                    if (two) load_item(b3);
+                    typename FO::Chunk n0{}, n1{};
+                    load_item(n0);
+                    if (two) load_item(n1);
                     const int a0 = pa * L.epp + al, a1 = a0 + L.epp;
                     const bool h0 = a0 < na, h1 = two && a1 < na;
-                    const int j0 = h0 ? C.act_begin[a0] : 0, j1 = h1 ? C.act_begin[a1] : 0;
+                    const int j0 = h0 ? a0 : 0, j1 = h1 ? a1 : 0;  // one entry per active expert
                     float v0 = 0.0f, v1 = 0.0f;
                     if (h0) {
                         typename FO::Frag f0;
@@ -1076,9 +1083,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     if (two) {
                         b0 = b2;
                         b1 = b3;
+                        b2 = n0;
+                        b3 = n1;
                     } else {  // b1 already holds the next task's first item
                         b0 = b1;
                         b1 = b2;
+                        b2 = b3;
+                        b3 = n0;
                     }
                 }
             } else {
