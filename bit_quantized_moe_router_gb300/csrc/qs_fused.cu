@@ -833,7 +833,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 const int a = cur.a, tt = cur.tt;
                 const int r = cur.rt * L.rpw + rl;
                 const uint8_t* grow = task_row(cur);
-                const int j0 = C.act_begin[a], ne = C.act_begin[a + 1] - j0;
+                // one token: active expert a holds sorted entry a and no other
+                const int j0 = MAXT == 1 ? a : C.act_begin[a], ne = MAXT == 1 ? 1 : C.act_begin[a + 1] - j0;
                 float gacc[MAXT], uacc[MAXT];
 #pragma unroll
                 for (int e = 0; e < MAXT; e++) gacc[e] = uacc[e] = 0.0f;
@@ -860,7 +861,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
 #pragma unroll
                         for (int e = 0; e < MAXT; e++) {
                             if (e < ne) {
-                                const int t = C.es_tok[j0 + e];
+                                const int t = MAXT == 1 ? 0 : C.es_tok[j0 + e];
                                 float dg, du;
                                 FO::dot2(gc, uc, c & 3, xqf + ((size_t)t * (H / 64) + c) * kFragWords, dg, du);
                                 gacc[e] += dg;
@@ -881,7 +882,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                             }
                         }
                         if (c0 == 0) {
-                            const float sx = C.xscale[C.es_tok[j0 + e]] * (1.0f / 32767.0f);
+                            const float sx = C.xscale[MAXT == 1 ? 0 : C.es_tok[j0 + e]] * (1.0f / 32767.0f);
                             P.xh[(size_t)(j0 + e) * F + tt * P.R + r] = silu(gv * sx) * (uv * sx);
                         }
                     }
