@@ -45,9 +45,8 @@ __device__ __forceinline__ void red_relaxed_add_u64(uint64_t* p, uint64_t v) {
 
 // ------------------------------------------------------------------ dense rows
 
-template <bool F32>
-__device__ __forceinline__ void load8(const uint8_t* p, float* v) {
-    if (F32) {
+__device__ __forceinline__ void load8(const uint8_t* p, bool f32, float* v) {
+    if (f32) {
         const float4 a = reinterpret_cast<const float4*>(p)[0];
         const float4 b = reinterpret_cast<const float4*>(p)[1];
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
@@ -59,11 +58,6 @@ __device__ __forceinline__ void load8(const uint8_t* p, float* v) {
         v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
         v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
     }
-}
-
-__device__ __forceinline__ void load8(const uint8_t* p, bool f32, float* v) {
-    if (f32) load8<true>(p, v);
-    else load8<false>(p, v);
 }
 
 // One warp: dot products of one dense row (K elements, fp32 or bf16, shared or global memory)
@@ -95,45 +89,6 @@ __device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int
 #pragma unroll
     for (int t = 0; t < MAXT; t++)
         if (t < T) acc[t] = warp_sum(acc[t]);
-}
-
-// Two bf16 rows (a gate row and an up row) against the same activations in one pass: each row's
-// sums are formed exactly as warp_dense_row forms them.
-template <int MAXT>
-__device__ __forceinline__ void warp_dense_rows2(const uint8_t* wa, const uint8_t* wb, int K, const uint8_t* act,
-                                                 bool a_f32, int T, float* acc_a, float* acc_b) {
-    const int lane = threadIdx.x & 31;
-    const int asz = a_f32 ? 4 : 2;
-#pragma unroll
-    for (int t = 0; t < MAXT; t++) acc_a[t] = acc_b[t] = 0.0f;
-#pragma unroll 2
-    for (int i = lane * 8; i < K; i += 256) {
-        float va[8], vb[8];
-        load8<false>(wa + (size_t)i * 2, va);
-        load8<false>(wb + (size_t)i * 2, vb);
-#pragma unroll
-        for (int t = 0; t < MAXT; t++) {
-            if (t < T) {
-                float av[8];
-                load8(act + ((size_t)t * K + i) * asz, a_f32, av);
-                float sa = acc_a[t], sb = acc_b[t];
-#pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    sa = fmaf(va[q], av[q], sa);
-                    sb = fmaf(vb[q], av[q], sb);
-                }
-                acc_a[t] = sa;
-                acc_b[t] = sb;
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < MAXT; t++) {
-        if (t < T) {
-            acc_a[t] = warp_sum(acc_a[t]);
-            acc_b[t] = warp_sum(acc_b[t]);
-        }
-    }
 }
 
 // ------------------------------------------------------------------ routing (one warp per token)
