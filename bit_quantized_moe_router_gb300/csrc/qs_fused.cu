@@ -904,9 +904,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
             }
         }
         // ---------------------------------------------------------- down rows: setup
-        // This warp's down items (task, pass) form one stream, loaded two items ahead.  The first
-        // two depend only on the routing: they are requested before the staging tasks and the
-        // waits for the staged h.
+        // This warp's down items (task, pass) form one stream, loaded two items ahead (four at one
+        // token, where passes go in pairs).  The first ones depend only on the routing: they are
+        // requested before the staging tasks and the waits for the staged h.
         const int al = L.cpf >= 32 ? 0 : lane / L.cpf;  // epp experts per pass, cpf lanes per expert row
         const int dc0 = L.cpf >= 32 ? lane : lane % L.cpf;
         const unsigned dgm = L.cpf >= 32 ? 0xffffffffu : (((1u << L.cpf) - 1u) << (lane & ~(L.cpf - 1)));
