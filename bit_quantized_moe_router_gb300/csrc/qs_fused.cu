@@ -707,8 +707,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                     uw = st + (size_t)(P.RS + r) * H * 2;
                 }
                 float ga[MAXT], ua[MAXT];
-                warp_dense_row<MAXT>(gw, false, H, xraw, x_f32, T, ga);
-                warp_dense_row<MAXT>(uw, false, H, xraw, x_f32, T, ua);
+                if (MAXT > 1) {  // several tokens: both rows in one pass over the activations
+                    warp_dense_rows2<MAXT>(gw, uw, H, xraw, x_f32, T, ga, ua);
+                } else {  // one token: one row at a time, four loads of each in flight
+                    warp_dense_row<MAXT>(gw, false, H, xraw, x_f32, T, ga);
+                    warp_dense_row<MAXT>(uw, false, H, xraw, x_f32, T, ua);
+                }
 #pragma unroll
                 for (int t = 0; t < MAXT; t++)
                     if (t < T && lane == t) P.xhs[(size_t)t * S + row] = silu(ga[t]) * ua[t];

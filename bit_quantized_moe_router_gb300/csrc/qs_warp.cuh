@@ -91,6 +91,45 @@ __device__ __forceinline__ void warp_dense_row(const uint8_t* w, bool w_f32, int
         if (t < T) acc[t] = warp_sum(acc[t]);
 }
 
+// Two bf16 rows (a gate row and an up row) against the same activations in one pass: each row's
+// sums are formed exactly as warp_dense_row forms them.
+template <int MAXT>
+__device__ __forceinline__ void warp_dense_rows2(const uint8_t* wa, const uint8_t* wb, int K, const uint8_t* act,
+                                                 bool a_f32, int T, float* acc_a, float* acc_b) {
+    const int lane = threadIdx.x & 31;
+    const int asz = a_f32 ? 4 : 2;
+#pragma unroll
+    for (int t = 0; t < MAXT; t++) acc_a[t] = acc_b[t] = 0.0f;
+#pragma unroll 2
+    for (int i = lane * 8; i < K; i += 256) {
+        float va[8], vb[8];
+        load8(wa + (size_t)i * 2, false, va);
+        load8(wb + (size_t)i * 2, false, vb);
+#pragma unroll
+        for (int t = 0; t < MAXT; t++) {
+            if (t < T) {
+                float av[8];
+                load8(act + ((size_t)t * K + i) * asz, a_f32, av);
+                float sa = acc_a[t], sb = acc_b[t];
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    sa = fmaf(va[q], av[q], sa);
+                    sb = fmaf(vb[q], av[q], sb);
+                }
+                acc_a[t] = sa;
+                acc_b[t] = sb;
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < MAXT; t++) {
+        if (t < T) {
+            acc_a[t] = warp_sum(acc_a[t]);
+            acc_b[t] = warp_sum(acc_b[t]);
+        }
+    }
+}
+
 // ------------------------------------------------------------------ routing (one warp per token)
 
 // Order-preserving map of a logit to an unsigned key, + 1 so that 0 means "none" (the largest
