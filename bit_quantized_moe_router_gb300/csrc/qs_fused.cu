@@ -1103,15 +1103,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_decode_kernel(const Fu
                 load_item(b2);
                 const int a = pa * L.epp + al;
                 if (a < na) {
+                    // the expert's entries two at a time: two independent dot chains against one
+                    // chunk (the same sums, the same order)
+                    const int je = C.act_begin[a + 1];
 #pragma unroll 1
-                    for (int j = C.act_begin[a]; j < C.act_begin[a + 1]; j++) {
-                        typename FO::Frag f;
-                        FO::load_frag(hqf + ((size_t)j * (F / 64) + dc0) * kFragWords, f);
-                        float v = FO::dot(b0, du, f);
+                    for (int j = C.act_begin[a]; j < je; j += 2) {
+                        const bool two = j + 1 < je;  // uniform over the lanes of this expert's row
+                        float v0, v1 = 0.0f;
+                        {
+                            typename FO::Frag f;
+                            FO::load_frag(hqf + ((size_t)j * (F / 64) + dc0) * kFragWords, f);
+                            v0 = FO::dot(b0, du, f);
+                        }
+                        if (two) {
+                            typename FO::Frag f;
+                            FO::load_frag(hqf + ((size_t)(j + 1) * (F / 64) + dc0) * kFragWords, f);
+                            v1 = FO::dot(b0, du, f);
+                        }
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1)
-                            if (o < L.cpf) v += __shfl_xor_sync(dgm, v, o);
-                        if (dc0 == 0) pb[j] = v * C.hscale[j];
+                        for (int o = 16; o > 0; o >>= 1) {
+                            if (o < L.cpf) {
+                                v0 += __shfl_xor_sync(dgm, v0, o);
+                                v1 += __shfl_xor_sync(dgm, v1, o);
+                            }
+                        }
+                        if (dc0 == 0) {
+                            pb[j] = v0 * C.hscale[j];
+                            if (two) pb[j + 1] = v1 * C.hscale[j + 1];
+                        }
                     }
                 }
                 b0 = b1;
