@@ -45,6 +45,7 @@
 #include "qs_internal.h"
 #include "qs_q2k.cuh"
 #include "qs_tc.cuh"
+#include "qs_warp.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -372,8 +373,15 @@ __global__ void __launch_bounds__(256) pf_topk_kernel(const float* __restrict__ 
         lt[e] = l;
     }
     __syncwarp();
-    topk_softmax_warp(lt, E, k, ids + (size_t)t * k, pw + (size_t)t * k);
-    if (lane < k) atomicAdd(&counts[ids[(size_t)t * k + lane]], 1);  // lane j wrote id j itself
+    int id;
+    float w;
+    if (E <= 256) warp_topk<8>(lt, E, k, id, w);  // each lane reads back the logits it stored
+    else warp_topk_stream(lt, E, k, id, w);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = id;
+        pw[(size_t)t * k + lane] = w;
+        atomicAdd(&counts[id], 1);
+    }
     if (wsig) {
         const uint4* xr = reinterpret_cast<const uint4*>(x + (size_t)t * H);
         const uint4* gr = reinterpret_cast<const uint4*>(wsig);
