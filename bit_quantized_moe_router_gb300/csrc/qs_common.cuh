@@ -29,8 +29,9 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) <= kHeaderBytes, "header too large");
 
-// Counters of the persistent decode kernel (tiles of logits, hs and h published; CTAs
-// that have left), zeroed by its last CTA out, and the counter of the wait test.
+// Counters of the persistent decode kernel (CTAs that have published their logits, hs and
+// h; CTAs that have left), never reset: every call adds gridDim to each, so a call finds its
+// targets from the exit count.  And the counter of the wait test.
 enum Counter { kCtrLogits = 0, kCtrHs = 1, kCtrExit = 2, kCtrTest = 3, kCtrH = 4 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -6,7 +6,7 @@
 // soon as this call's CTA there leaves.  Before it waits for the previous grid
 // (griddepcontrol.wait) the producer warp only prefetches weights into L2; no
 // thread touches x, the workspace or the output before that wait.  A CTA has
-// one producer warp and 16 consumer warps.  The producer streams the CTA's
+// one producer warp and 15 consumer warps.  The producer streams the CTA's
 // routing-independent tiles from HBM into a ring of 21 KB shared-memory stages
 // with bulk asynchronous copies (TMA engine): one "full" mbarrier per stage
 // counts the bytes in, one "empty" mbarrier per stage tells the producer the
@@ -15,6 +15,8 @@
 //
 //   router rows (fp32)  |  shared gate/up rows (bf16)  |  [routed gate/up rows (Q2_K)]  |  [down groups]
 //
+// (For one token, or a ring of fewer than three stages, group B reads the shared gate/up
+// rows from global memory instead, prefetched into L2 at the start.)
 // The routed gate/up rows and the down groups (RD output rows: the shared
 // expert's bf16 down rows and every active expert's Q2_K down rows) are
 // numbered as tiles but do not pass through the ring: the warps that use them
@@ -28,7 +30,7 @@
 // different phases at once and nothing waits on a CTA-wide barrier:
 //   group A (warps 0-7):  router rows -> logits; then the routing
 //                         (top-k, softmax, grouping of the T*k entries by expert)
-//   group B (warps 8-15): x scales, int16 x and sigmoid gates; shared gate/up rows -> hs
+//   group B (warps 8-14): x scales, int16 x and sigmoid gates; shared gate/up rows -> hs
 //   then every warp, round robin over the CTA's remaining tasks:
 //     routed gate/up rows -> h;  staging of hs and of each entry's int16 h;
 //     down rows: shared-expert down row + every active expert's down row -> out,
