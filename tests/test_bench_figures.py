@@ -46,3 +46,21 @@ def test_prefill_2048_flops():
 def test_aggregate_throughput_counts_every_rank():
     # four replicas of 8 tokens x 100 steps over the slowest rank's 0.5 s
     assert bench.aggregate_throughput(8, 100, 4, 0.5) == 6400.0
+
+
+def test_recorded_traffic_only_for_the_sources_it_was_taken_on(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only while the kernel sources hash to
+    the value recorded beside it; an edited source (or no summary) gives None."""
+    import hashlib
+    src = tmp_path / "k.cu"
+    src.write_text("kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    digest = hashlib.sha256(b"kernel v1\n").hexdigest()[:16]
+    (tmp_path / "profiles" / "fused_decode_kernel_w.md").write_text(
+        f"summary\n\ntraffic_bytes_per_launch: 12345\nkernel_sources_sha256_16: {digest}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", ("k.cu",))
+    assert bench.recorded_traffic("w") == 12345
+    assert bench.recorded_traffic("other") is None
+    src.write_text("kernel v2\n")
+    assert bench.recorded_traffic("w") is None
